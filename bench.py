@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of one tree-verify step on GB300.
+
+A step is one pass of the whole verify path over one batch: draft-KV scatter,
+KV index marshaling, tree-mask packing and tree-verify attention (with its
+split merge). Default workload: 8 requests, prefixes U{1024..4096},
+16-node draft trees (branching <= 3), 8 heads, 65536-slot pool.
+
+Timing: each of the four calls is captured once as a CUDA graph; a timed
+step replays the four graphs with CUDA events between them on the launching
+stream, so the step time and the verify call's own time come from the same
+events. L2 is flushed between steps by writing a 256 MiB buffer (outside the
+events). Inputs are resident in HBM when the timed region starts.
+
+value = KV bytes the steps had to read (every prefix + draft row of every
+request once, 1152 B per row) / device time, summed over ranks / max time.
+e2e = the same metric through the public API with host buffers: pinned
+host -> device copies of the step's inputs, the four calls, and the device
+-> host read of out and lse, all inside the timed region.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample (one request of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify MLA attention µs/call and KV GB/s (% of GB300 HBM roofline)"
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def alg_cost(w):
+    """Algorithmic bytes and flops of one verify call: every key row once,
+    its index, the mask bytes, q in, out and lse out; flops over visible
+    (row, key) pairs only."""
+    H = w.heads
+    qo = w.qo_indptr.tolist()
+    byts, flops = 0, 0
+    for b in range(w.batch):
+        n, P = w.tree_sizes[b], w.prefix_lens[b]
+        L = P + n
+        byts += L * 1152 + L * 4 + n * L + n * H * (1152 + 1024 + 4)
+        par = w.parents[qo[b]:qo[b + 1]].tolist()
+        depth = []
+        for i, p in enumerate(par):
+            depth.append(1 if p < 0 else depth[p] + 1)
+        flops += 2 * 1088 * H * (n * P + sum(depth))
+    return byts, flops
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0])); mx.append(float(f[1]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decode_mla_tree_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("verify") or name.endswith((".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(kernel)
+        if e and e.get("source_hash") == _kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(cid, budget_s, one_request=False, steps=None):
+    """Time the fp64 oracle on this host's cores; returns (GB/s, seconds, sample text)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decode_mla_tree_gb300 import workloads as W
+
+    w = W.config(cid)
+    pool_bits = w.dense_pool().view(torch.int16).numpy().view(np.uint16)
+    q_bits = w.q.view(torch.int16).numpy().view(np.uint16)
+    dkv = w.draft_kv.view(torch.int16).numpy().view(np.uint16)
+    qo = w.qo_indptr.numpy()
+
+    def one_step(b=None):
+        pool = oracle.draft_kv_scatter(pool_bits, dkv, w.out_cache_loc)
+        kv_indices, kv_indptr = oracle.kv_indices_build(w.prefix_indices, w.prefix_indptr,
+                                                        w.out_cache_loc, w.qo_indptr)
+        mask_indptr, mask = oracle.tree_mask_pack(w.parents, w.qo_indptr, kv_indptr)
+        rows = None
+        if b is not None:
+            rows = [(t, h) for t in range(qo[b], qo[b + 1]) for h in range(w.heads)]
+        oracle.verify_attention(q_bits, pool, kv_indices, kv_indptr, w.qo_indptr, mask,
+                                mask_indptr, w.heads, w.sm_scale, rows=rows)
+        if b is None:
+            return w.kv_bytes()
+        return (w.prefix_lens[b] + w.tree_sizes[b]) * 1152
+
+    done, t0, k = 0, time.perf_counter(), 0
+    while True:
+        b = (k % w.batch) if one_request else None
+        done += one_step(b)
+        k += 1
+        el = time.perf_counter() - t0
+        if steps is not None and k >= steps:
+            break
+        if steps is None and el >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    sample = ("%d oracle steps of %s" % (k, "one request each (all its rows)" if one_request
+                                          else "the whole batch"))
+    return done / el / 1e9, el, sample, k
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = len(os.sched_getaffinity(0))
+    from speculative_decode_mla_tree_gb300 import workloads as W
+    cpu_baseline(args.config, 0, one_request=True, steps=max(1, args.warmup))
+    gbs, el, sample, k = cpu_baseline(args.config, 0, one_request=True, steps=args.steps)
+    w = W.config(args.config)
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / k * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": W.CONFIG_NAMES[args.config], "sample": "one request per step"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from speculative_decode_mla_tree_gb300 import abi, workloads as W
+    from speculative_decode_mla_tree_gb300.step import VerifyStep
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    __graft_entry__.build()
+
+    w = W.config(args.config)
+    st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            st.run()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, "device status %d" % int(st.status.item())
+
+    calls = [lambda: abi.mla_tree_draft_kv_scatter(st.draft_kv, st.out_cache_loc, st.pool, st.status),
+             lambda: abi.mla_tree_kv_indices_build(st.prefix_indices, st.prefix_indptr, st.out_cache_loc,
+                                                   st.qo_indptr, st.kv_indices, st.kv_indptr, st.status),
+             lambda: abi.tree_mask_pack(st.parents, st.qo_indptr, st.kv_indptr, st.mask_indptr, st.mask,
+                                        st.status),
+             lambda: st.verify()]
+    graphs = []
+    for c in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            c()
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def step(ev):
+        ev[0].record(stream)
+        for i, g in enumerate(graphs):
+            g.replay()
+            ev[i + 1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step([torch.cuda.Event(enable_timing=True) for _ in range(5)])
+    torch.cuda.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    idx = vis.split(",")[local] if vis and vis.split(",")[local].strip().isdigit() else str(local)
+    clocks = ClockSampler(idx)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            step(events[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in events]
+    call_ms = [[e[i].elapsed_time(e[i + 1]) for e in events] for i in range(4)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert int(st.status.item()) == 0
+
+    kv_bytes = w.kv_bytes()
+    value = world * args.steps * kv_bytes / (total_ms * 1e-3) / 1e9
+    byts, flops = alg_cost(w)
+    verify_ms = statistics.mean(call_ms[3])
+    hbm, tf_burst, tf_sus, which = _peaks()
+    achieved_gbs = byts / (verify_ms * 1e-3) / 1e9
+    achieved_tf = flops / (verify_ms * 1e-3) / 1e12
+    t_hbm, t_tc = byts / (hbm * 1e9), flops / (tf_burst * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    launches_verify = abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, args.max_splits, args.path)
+    launches = args.steps * (3 + launches_verify)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = [(d, h.pin_memory()) for d, h in st.inputs()]
+        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        lse_h = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for k in range(args.warmup + args.steps):
+                flush.fill_(float(k))
+                e = ev[k - args.warmup] if k >= args.warmup else None
+                if e:
+                    e[0].record(stream)
+                for d, h in host_in:
+                    d.copy_(h, non_blocking=True)
+                st.run()
+                out_h.copy_(st.out, non_blocking=True)
+                lse_h.copy_(st.lse, non_blocking=True)
+                if e:
+                    e[1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * args.steps * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, el, sample, k = cpu_baseline(args.config, args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": sample + " (%.1f s)" % el}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "us_per_call": verify_ms * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": W.CONFIG_NAMES[args.config], "batch": w.batch, "heads": w.heads,
+                       "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
+                       "path": ["auto", "simt", "tensor-core"][args.path],
+                       "max_splits": args.max_splits,
+                       "l2": "flushed between steps (256 MiB write outside the events)",
+                       "timing": "per-call CUDA graphs, CUDA events on the launching stream"},
+            "step_ms": {"scatter": statistics.mean(call_ms[0]), "kv_indices": statistics.mean(call_ms[1]),
+                        "mask_pack": statistics.mean(call_ms[2]), "verify": verify_ms,
+                        "verify_p10": sorted(call_ms[3])[len(call_ms[3]) // 10],
+                        "verify_p90": sorted(call_ms[3])[(9 * len(call_ms[3])) // 10]},
+            "roofline": {"kernel": "mla_tree_verify (all launches of the call)", "bound": bound,
+                         "achieved": achieved_gbs if bound == "hbm" else achieved_tf,
+                         "peak": hbm if bound == "hbm" else tf_burst,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                         "frac": (achieved_gbs / hbm) if bound == "hbm" else (achieved_tf / tf_burst),
+                         "traffic": _traffic("verify"), "peak_source": which,
+                         "alg_bytes_per_launch": byts, "alg_flops_per_launch": flops,
+                         "hbm_frac": achieved_gbs / hbm, "tensor_frac": achieved_tf / tf_burst},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,251 @@
+// Boundary kernels of the verify step: draft-KV scatter, KV index
+// marshaling and tree-mask packing. Integer / byte work only: HBM-write
+// bound, results bit-exact.
+//
+// "The Moment of Truth: Flipping the Switch on a Custom CUDA Verify Kernel",
+// section "The Long Road to Parity": draft KV is written to out_cache_loc
+// and the index array is prefix slots followed by draft slots, with the mask
+// row stride prefix + draft. "The Pivot to Live Cutover", section "The
+// Technical Investigation": flat mask with per-sequence offsets.
+#include "mt_common.cuh"
+#include "mt_internal.h"
+
+namespace mt {
+
+// ---------------------------------------------------------------- scatter
+
+// One thread per 16-byte vector of a 1152-byte row: a warp moves 512
+// contiguous bytes of one source row into one pool row.
+__global__ void __launch_bounds__(256) draft_kv_scatter_vec(const uint4* __restrict__ src,
+                                                            int64_t src_stride_vec,
+                                                            const int32_t* __restrict__ loc,
+                                                            int total_q, uint4* __restrict__ kv,
+                                                            int64_t num_slots, int32_t* status) {
+  const int64_t total = (int64_t)total_q * kRowVec;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / kRowVec;
+    const int v = (int)(idx - t * kRowVec);
+    const int32_t slot = loc[t];
+    if (slot < 0 || slot >= num_slots) {
+      if (v == 0) flag(status, MT_DEV_BAD_SLOT);
+      continue;
+    }
+    kv[(int64_t)slot * kRowVec + v] = src[t * src_stride_vec + v];
+  }
+}
+
+// Fallback for sources that are not 16-byte aligned: 2-byte copies.
+__global__ void __launch_bounds__(256) draft_kv_scatter_u16(const uint16_t* __restrict__ src,
+                                                            int64_t src_stride,
+                                                            const int32_t* __restrict__ loc,
+                                                            int total_q, uint16_t* __restrict__ kv,
+                                                            int64_t num_slots, int32_t* status) {
+  const int64_t total = (int64_t)total_q * kDqk;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / kDqk;
+    const int d = (int)(idx - t * kDqk);
+    const int32_t slot = loc[t];
+    if (slot < 0 || slot >= num_slots) {
+      if (d == 0) flag(status, MT_DEV_BAD_SLOT);
+      continue;
+    }
+    kv[(int64_t)slot * kDqk + d] = src[t * src_stride + d];
+  }
+}
+
+cudaError_t launch_draft_kv_scatter(const uint16_t* src, int64_t src_stride, const int32_t* loc,
+                                    int total_q, uint16_t* kv, int64_t num_slots, int32_t* status,
+                                    int num_sms, cudaStream_t stream) {
+  const bool vec = ((uintptr_t)src % 16 == 0) && ((uintptr_t)kv % 16 == 0) && (src_stride % 8 == 0);
+  const int64_t work = (int64_t)total_q * (vec ? kRowVec : kDqk);
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (vec)
+    draft_kv_scatter_vec<<<(unsigned)blocks, 256, 0, stream>>>(
+        (const uint4*)src, src_stride / 8, loc, total_q, (uint4*)kv, num_slots, status);
+  else
+    draft_kv_scatter_u16<<<(unsigned)blocks, 256, 0, stream>>>(src, src_stride, loc, total_q, kv,
+                                                               num_slots, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- kv indices
+
+// grid (chunks, batch): chunk c of request b copies positions j = c*256+tid,
+// stepping by chunks*256.
+__global__ void __launch_bounds__(256) kv_indices_build_kernel(
+    const int32_t* __restrict__ pidx, int64_t pidx_len, const int32_t* __restrict__ pptr,
+    const int32_t* __restrict__ loc, const int32_t* __restrict__ qptr, int batch, int total_q,
+    int32_t* __restrict__ kv_indices, int64_t capacity, int32_t* __restrict__ kv_indptr,
+    int32_t* status) {
+  const int b = blockIdx.y;
+  const int64_t p0 = pptr[b], p1 = pptr[b + 1];
+  const int64_t q0 = qptr[b], q1 = qptr[b + 1];
+  const int64_t base = p0 + q0;
+  const int64_t P = p1 - p0, n = q1 - q0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    kv_indptr[b] = (int32_t)base;
+    if (b == batch - 1) {
+      kv_indptr[batch] = (int32_t)(p1 + q1);
+      if (q1 != total_q) flag(status, MT_DEV_BAD_INDPTR);
+    }
+  }
+  if (P < 0 || n < 0 || p0 < 0 || q0 < 0 || p1 > pidx_len || q1 > total_q ||
+      base + P + n > capacity || base + P + n > 0x7fffffffLL) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
+    return;
+  }
+  const int64_t L = P + n;
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < L;
+       j += (int64_t)gridDim.x * blockDim.x)
+    kv_indices[base + j] = j < P ? pidx[p0 + j] : loc[q0 + (j - P)];
+}
+
+cudaError_t launch_kv_indices_build(const int32_t* pidx, int64_t pidx_len, const int32_t* pptr,
+                                    const int32_t* loc, const int32_t* qptr, int batch, int total_q,
+                                    int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                                    int32_t* status, int num_sms, cudaStream_t stream) {
+  int chunks = (2 * num_sms + batch - 1) / batch;
+  if (chunks < 1) chunks = 1;
+  if (chunks > 256) chunks = 256;
+  dim3 grid(chunks, batch);
+  kv_indices_build_kernel<<<grid, 256, 0, stream>>>(pidx, pidx_len, pptr, loc, qptr, batch, total_q,
+                                                    kv_indices, capacity, kv_indptr, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- tree mask
+
+// grid (row groups, batch). Each CTA: compute its request's mask offset by
+// summing n*L over earlier requests; for each of its rows, walk the parent
+// chain once into a shared bitset, then write the row: prefix bytes 1, draft
+// byte k = bit k. Interior 16-byte chunks go out as one vector store; the
+// head and tail bytes of a row (which may share a 16-byte chunk with the
+// neighbouring row) are written byte by byte so no byte has two writers.
+constexpr int kMaskThreads = 256;
+
+__device__ __forceinline__ uint8_t mask_byte(int64_t col, int64_t P, const uint32_t* bits) {
+  if (col < P) return 1;
+  const int64_t k = col - P;
+  return (uint8_t)((bits[k >> 5] >> (k & 31)) & 1u);
+}
+
+__global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
+    const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
+    const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ mask_indptr,
+    uint8_t* __restrict__ mask, int64_t capacity, int32_t* status) {
+  __shared__ uint32_t bits[MT_MAX_TREE / 32];
+  __shared__ long long s_base;
+  __shared__ int s_bad;
+  const int b = blockIdx.y;
+  if (threadIdx.x == 0) {
+    long long base = 0;
+    int bad = 0;
+    for (int r = 0; r < b; ++r) {
+      const long long n = (long long)qptr[r + 1] - qptr[r];
+      const long long L = (long long)kptr[r + 1] - kptr[r];
+      if (n < 0 || L < n) bad = 1;
+      base += n * L;
+    }
+    s_base = base;
+    s_bad = bad;
+    if (b == 0 && blockIdx.x == 0) {
+      // Offsets for every request (serial: batch is small).
+      long long acc = 0;
+      mask_indptr[0] = 0;
+      for (int r = 0; r < batch; ++r) {
+        const long long n = (long long)qptr[r + 1] - qptr[r];
+        const long long L = (long long)kptr[r + 1] - kptr[r];
+        acc += (n >= 0 && L >= n) ? n * L : 0;
+        mask_indptr[r + 1] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t q0 = qptr[b];
+  const int64_t n = (int64_t)qptr[b + 1] - q0;
+  const int64_t L = (int64_t)kptr[b + 1] - kptr[b];
+  const int64_t P = L - n;
+  const int64_t base = s_base;
+  if (s_bad || n < 0 || P < 0 || q0 < 0 || q0 + n > total_q || base + n * L > capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
+    return;
+  }
+  if (n > MT_MAX_TREE) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_TREE_TOO_BIG);
+    return;
+  }
+  const int words = (int)((n + 31) >> 5);
+  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+    for (int w = threadIdx.x; w < words; w += blockDim.x) bits[w] = 0u;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // Ancestor-or-self walk; parents strictly decrease, so at most n steps.
+      int64_t k = i;
+      while (k >= 0) {
+        bits[k >> 5] |= 1u << (k & 31);
+        const int32_t p = parents[q0 + k];
+        if (p < -1 || p >= k) {
+          flag(status, MT_DEV_BAD_PARENT);
+          break;
+        }
+        k = p;
+      }
+    }
+    __syncthreads();
+    uint8_t* row = mask + base + i * L;
+    const uintptr_t a = (uintptr_t)row, e = a + (uintptr_t)L;
+    uintptr_t a0 = (a + 15) & ~(uintptr_t)15;
+    uintptr_t a1 = e & ~(uintptr_t)15;
+    if (a0 > e) a0 = e;
+    if (a1 < a0) a1 = a0;
+    // head and tail bytes
+    const int64_t head = (int64_t)(a0 - a), tail = (int64_t)(e - a1);
+    for (int64_t c = threadIdx.x; c < head + tail; c += blockDim.x) {
+      const int64_t col = c < head ? c : (int64_t)(a1 - a) + (c - head);
+      row[col] = mask_byte(col, P, bits);
+    }
+    // interior 16-byte chunks
+    const int64_t chunks = (int64_t)(a1 - a0) >> 4;
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const int64_t col0 = (int64_t)(a0 - a) + (c << 4);
+      uint4 v;
+      if (col0 + 16 <= P) {
+        v = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
+      } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t x = 0;
+#pragma unroll
+          for (int y = 0; y < 4; ++y) x |= (uint32_t)mask_byte(col0 + q * 4 + y, P, bits) << (8 * y);
+          w[q] = x;
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *(uint4*)(row + col0) = v;
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_tree_mask_pack(const int32_t* parents, const int32_t* qptr, const int32_t* kptr,
+                                  int batch, int total_q, int64_t* mask_indptr, uint8_t* mask,
+                                  int64_t capacity, int32_t* status, int num_sms,
+                                  cudaStream_t stream) {
+  // Enough row groups to cover the largest tree for moderate batches, and
+  // at least ~2 CTAs per SM overall.
+  int groups = (2 * num_sms + batch - 1) / batch;
+  if (groups < 1) groups = 1;
+  if (groups > 64) groups = 64;
+  dim3 grid(groups, batch);
+  tree_mask_pack_kernel<<<grid, kMaskThreads, 0, stream>>>(parents, qptr, kptr, batch, total_q,
+                                                           mask_indptr, mask, capacity, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mt

@@ -1,0 +1,63 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mt {
+
+// Arguments of one verify call, passed by value to the attention kernels.
+struct VerifyArgs {
+  const uint16_t* q;            // bf16 [total_q, heads, 576]
+  const uint16_t* kv;           // bf16 [num_slots, 576]
+  int64_t num_slots;
+  const int32_t* kv_indices;
+  int64_t kv_len;
+  const int32_t* kv_indptr;
+  const int32_t* qo_indptr;
+  const uint8_t* mask;
+  int64_t mask_len;
+  const int64_t* mask_indptr;
+  int batch, total_q, heads;
+  float sm_scale;
+  uint16_t* out;                // bf16 [total_q, heads, 512]
+  float* lse;                   // fp32 [total_q, heads]
+  int max_splits;               // capacity of the partial buffers
+  int32_t* status;
+  // workspace views
+  int32_t* ws_nsplit;           // [batch] split count each request used
+  float* ws_lse;                // [max_splits][total_q*heads]
+  float* ws_o;                  // [max_splits][total_q*heads][512]
+  int32_t* ws_counter;          // [tiles] arrival counters (tensor-core path)
+  int64_t ws_counter_len;
+};
+
+struct WorkspaceLayout {
+  size_t nsplit_off, lse_off, o_off, counter_off, total;
+  int64_t counter_len;
+};
+
+WorkspaceLayout workspace_layout(int batch, int total_q, int heads, int max_splits);
+int auto_max_splits(int batch, int total_q, int heads, int num_sms);
+
+cudaError_t launch_draft_kv_scatter(const uint16_t* src, int64_t src_stride, const int32_t* loc,
+                                    int total_q, uint16_t* kv, int64_t num_slots, int32_t* status,
+                                    int num_sms, cudaStream_t stream);
+cudaError_t launch_kv_indices_build(const int32_t* pidx, int64_t pidx_len, const int32_t* pptr,
+                                    const int32_t* loc,
+                                    const int32_t* qptr, int batch, int total_q,
+                                    int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                                    int32_t* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_tree_mask_pack(const int32_t* parents, const int32_t* qptr, const int32_t* kptr,
+                                  int batch, int total_q, int64_t* mask_indptr, uint8_t* mask,
+                                  int64_t capacity, int32_t* status, int num_sms,
+                                  cudaStream_t stream);
+
+cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream);
+// Tensor-core path; returns cudaErrorNotSupported when it cannot serve `a`.
+cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stream);
+// Kernels one tensor-core verify call launches (0 when that path cannot serve it).
+int verify_tc_launches(int batch, int total_q, int heads, int max_splits);
+
+}  // namespace mt

@@ -1,0 +1,227 @@
+// Warp-shuffle (SIMT) tree-verify attention and the split-KV LSE merge.
+//
+// The path for small trees, where heads x draft rows cannot fill a tensor-core
+// tile (the pages' live call had 9 rows x 8 heads = 72: "Flipping the
+// Switch", section "The Long Road to Parity"). Split-KV flash-decode with a
+// log-sum-exp merge, after "Flipping the Switch", section "The Broader
+// Context".
+//
+// One warp owns one draft token and up to kRows heads of it, for one KV
+// split. Lane l holds latent dims [16 l, 16 l + 16) and rope dims
+// [512 + 2 l, 512 + 2 l + 2) of the query rows, so one pool row is read
+// with two 16-byte loads and one 4-byte load per lane (1152 contiguous bytes
+// per warp) and serves both the score (all 576 dims) and the value update
+// (the 512 latent dims the lane already holds). Scores are reduced with xor
+// shuffles, so every lane holds the same bits; the online softmax runs in
+// the log2 domain with sm_scale * log2(e) folded into q.
+#include <math.h>
+
+#include "mt_common.cuh"
+#include "mt_internal.h"
+
+namespace mt {
+
+constexpr int kRows = 4;          // heads per warp
+constexpr int kWarps = 4;         // warps per CTA
+constexpr int kMinChunk = 256;    // smallest KV split worth a warp
+
+__device__ __forceinline__ int simt_splits(int L, int max_splits, int* chunk) {
+  int c = (L + max_splits - 1) / max_splits;
+  if (c < kMinChunk) c = kMinChunk;
+  *chunk = c;
+  const int s = (L + c - 1) / c;
+  return s < 1 ? 1 : s;
+}
+
+__device__ __forceinline__ void load_row18(const uint16_t* row, int lane, float scale, float* f) {
+  const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(row) + 2 * lane);
+  const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(row) + 2 * lane + 1);
+  const uint32_t rp = __ldg(reinterpret_cast<const uint32_t*>(row + kDv) + lane);
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    f[2 * e] = bf16_lo(w[e]) * scale;
+    f[2 * e + 1] = bf16_hi(w[e]) * scale;
+  }
+  f[16] = bf16_lo(rp) * scale;
+  f[17] = bf16_hi(rp) * scale;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int hg_count = (a.heads + kRows - 1) / kRows;
+  const int64_t t = wid / hg_count;
+  const int h0 = (int)(wid - t * hg_count) * kRows;
+  if (t >= a.total_q) return;
+  const int split = blockIdx.y;
+  const int b = find_request(a.qo_indptr, a.batch, t);
+  const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
+                                 a.mask_len, a.total_q);
+  if (!g.ok || t < g.q0 || t >= g.q0 + g.n) {
+    if (lane == 0 && split == 0) flag(a.status, MT_DEV_BAD_INDPTR);
+    return;
+  }
+  int chunk;
+  const int S = simt_splits(g.L, a.max_splits, &chunk);
+  if (split == 0 && lane == 0 && t == g.q0 && h0 == 0) a.ws_nsplit[b] = S;
+  if (split >= S) return;
+  const int j0 = split * chunk;
+  const int j1 = min(g.L, j0 + chunk);
+
+  const float qscale = a.sm_scale * kLog2e;
+  float qv[kRows][18];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int h = h0 + r;
+    if (h < a.heads) {
+      load_row18(a.q + ((int64_t)t * a.heads + h) * kDqk, lane, qscale, qv[r]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 18; ++e) qv[r][e] = 0.f;
+    }
+  }
+
+  float m[kRows], l[kRows], acc[kRows][16];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[r][e] = 0.f;
+  }
+
+  const uint8_t* mrow = a.mask + g.mask0 + (t - g.q0) * (int64_t)g.L;
+  const int32_t* idx = a.kv_indices + g.kv0;
+  for (int j = j0; j < j1; ++j) {
+    const int32_t slot = __ldg(idx + j);
+    if (slot < 0 || slot >= a.num_slots) {
+      if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
+      continue;
+    }
+    if (!__ldg(mrow + j)) continue;
+    float kf[18];
+    load_row18(a.kv + (int64_t)slot * kDqk, lane, 1.f, kf);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < 18; ++e) d = fmaf(qv[r][e], kf[e], d);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (d > m[r]) {
+        const float c = exp2f(m[r] - d);
+        l[r] *= c;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[r][e] *= c;
+        m[r] = d;
+      }
+      const float p = exp2f(d - m[r]);
+      l[r] += p;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[r][e] = fmaf(p, kf[e], acc[r][e]);
+    }
+  }
+
+  const int64_t R = (int64_t)a.total_q * a.heads;
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int h = h0 + r;
+    if (h >= a.heads) continue;
+    const int64_t row = t * a.heads + h;
+    const bool any = l[r] > 0.f;
+    const float inv = any ? 1.f / l[r] : 0.f;
+    const float row_lse = any ? (m[r] + log2f(l[r])) * kLn2 : -INFINITY;
+    if (S == 1) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[r][2 * e] * inv, acc[r][2 * e + 1] * inv);
+        w[e] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv) + 2 * lane;
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      if (lane == 0) a.lse[row] = row_lse;
+    } else {
+      float4* dst = reinterpret_cast<float4*>(a.ws_o + ((int64_t)split * R + row) * kDv) + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dst[e] = make_float4(acc[r][4 * e] * inv, acc[r][4 * e + 1] * inv, acc[r][4 * e + 2] * inv,
+                             acc[r][4 * e + 3] * inv);
+      if (lane == 0) a.ws_lse[(int64_t)split * R + row] = row_lse;
+    }
+  }
+}
+
+cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream) {
+  (void)num_sms;
+  const int hg_count = (a.heads + kRows - 1) / kRows;
+  const int64_t warps = (int64_t)a.total_q * hg_count;
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
+  dim3 grid((unsigned)blocks, (unsigned)a.max_splits);
+  verify_simt_kernel<<<grid, kWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- merge
+
+// One warp per (token, head) row, lane l owns output dims [16 l, 16 l + 16):
+//   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
+// Requests that ran unsplit (ws_nsplit[b] == 1) were finished in place.
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const VerifyArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t R = (int64_t)a.total_q * a.heads;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (row >= R) return;
+  const int64_t t = row / a.heads;
+  const int b = find_request(a.qo_indptr, a.batch, t);
+  const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
+                                 a.mask_len, a.total_q);
+  if (!g.ok || t < g.q0 || t >= g.q0 + g.n) return;
+  const int S = a.ws_nsplit[b];
+  if (S <= 1 || S > a.max_splits) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < S; ++s) mx = fmaxf(mx, a.ws_lse[(int64_t)s * R + row]);
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  float tot = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float ls = a.ws_lse[(int64_t)s * R + row];
+      if (ls == -INFINITY) continue;
+      const float w = exp2f((ls - mx) * kLog2e);
+      tot += w;
+      const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((int64_t)s * R + row) * kDv) + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 v = src[e];
+        acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
+        acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
+      }
+    }
+  }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  uint32_t w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    w[e] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv) + 2 * lane;
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  if (lane == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+}
+
+cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
+  const int64_t R = (int64_t)a.total_q * a.heads;
+  const int64_t blocks = (R + kWarps - 1) / kWarps;
+  lse_merge_kernel<<<(unsigned)blocks, kWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mt

@@ -198,7 +198,7 @@ def make_workload(name, heads, prefix_lens, tree_rules, tree_sizes, num_slots, s
         prefix_indices=torch.cat(prefix_indices).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         out_cache_loc=torch.cat(out_cache_loc).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         q=q, draft_kv=draft_kv, pool_slots=slots, pool_rows=pool_rows,
-        meta={"seed": seed, "rules": list(tree_rules)},
+        meta={"seed": seed, "rules": list(tree_rules) if tree_rules else None},
     )
 
 

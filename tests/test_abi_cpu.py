@@ -1,0 +1,91 @@
+"""The C-ABI library loads, exports every function its header declares, and
+rejects bad host-side arguments before touching the GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from speculative_decode_mla_tree_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build_library()
+    return abi.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mla_tree.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(?:int|size_t|const char\*)\s+(\w+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    assert set(names) == set(abi.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mla_tree_abi_version() == 100
+    for code in (0, -1, -2, -3, -4):
+        assert lib.mla_tree_status_string(code).decode() not in ("", "unknown status")
+
+
+def test_host_argument_checks(lib):
+    null = None
+    # verify: zero heads, negative sizes, bad path, non-finite scale
+    args = [null, null, 0, null, 0, null, null, null, 0, null, 1, 1, 0, 1.0,
+            null, null, null, 0, 0, 0, null, null]
+    assert lib.mla_tree_verify(*args) == abi.MT_EINVAL
+    args[12] = 8; args[19] = 3
+    assert lib.mla_tree_verify(*args) == abi.MT_EINVAL
+    args[19] = 0; args[13] = float("nan")
+    assert lib.mla_tree_verify(*args) == abi.MT_EINVAL
+    args[13] = 1.0; args[18] = 5000
+    assert lib.mla_tree_verify(*args) == abi.MT_EINVAL
+    # empty batch is a successful no-op
+    args[18] = 0; args[10] = 0
+    assert lib.mla_tree_verify(*args) == abi.MT_OK
+    # null pointers with work to do
+    args[10] = 1
+    assert lib.mla_tree_verify(*args) == abi.MT_EINVAL
+    # misaligned q (odd address) with otherwise plausible pointers
+    fake = 4096
+    args2 = [fake + 2, fake, 10, fake, 10, fake, fake, fake, 10, fake, 1, 1, 8, 1.0,
+             fake, fake, fake, 1 << 20, 0, 0, null, null]
+    assert lib.mla_tree_verify(*args2) == abi.MT_EINVAL
+    # misaligned / too small workspace
+    args2[0] = fake; args2[16] = fake + 8
+    assert lib.mla_tree_verify(*args2) == abi.MT_EWORKSPACE
+    args2[16] = fake; args2[17] = 16
+    assert lib.mla_tree_verify(*args2) == abi.MT_EWORKSPACE
+    # marshaling entry points
+    assert lib.mla_tree_draft_kv_scatter(null, 100, null, 1, null, 10, null, null) == abi.MT_EINVAL
+    assert lib.mla_tree_draft_kv_scatter(null, 576, null, 0, null, 10, null, null) == abi.MT_OK
+    assert lib.mla_tree_kv_indices_build(null, 0, null, null, null, -1, 0, null, 0, null, null, null) == abi.MT_EINVAL
+    assert lib.mla_tree_kv_indices_build(null, 0, null, null, null, 2, 4, null, 0, null, null, null) == abi.MT_EINVAL
+    assert lib.tree_mask_pack(null, null, null, 0, 0, null, null, 0, null, null) == abi.MT_OK
+    assert lib.tree_mask_pack(null, null, null, 1, 3, null, null, 0, null, null) == abi.MT_EINVAL
+
+
+def test_workspace_size_grows_with_splits(lib):
+    a = lib.mla_tree_verify_workspace_bytes(8, 128, 8, 1)
+    b = lib.mla_tree_verify_workspace_bytes(8, 128, 8, 64)
+    assert 0 < a < b
+    assert b >= 64 * 128 * 8 * 513 * 4
+    assert lib.mla_tree_verify_workspace_bytes(8, 128, 8, 5000) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(abi.MlaTreeError):
+        abi._ptr(torch.zeros(4), None, "x")

@@ -53,7 +53,9 @@ enum {
   MT_EINVAL = -1,        /* bad pointer, size, alignment or scalar */
   MT_EUNSUPPORTED = -2,  /* valid request this build cannot serve */
   MT_EWORKSPACE = -3,    /* workspace missing, misaligned or too small */
-  MT_ECUDA = -4          /* a CUDA runtime call or launch failed */
+  MT_ECUDA = -4,         /* a CUDA runtime call or launch failed */
+  MT_ESCRATCH = -5       /* needs more scratch than mla_tree_verify_noalloc's
+                            built-in MT_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Device-side status bits, OR-ed into *dev_status by the kernels. */
@@ -186,6 +188,35 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
                     mt_bf16* out, float* lse,
                     void* workspace, size_t workspace_bytes, int max_splits, int path,
                     int32_t* dev_status, mt_stream_t stream);
+
+/*
+ * mla_tree_verify without a caller-provided workspace. The paper has no
+ * counterpart: this exists for embedders. Some callers cannot allocate
+ * device memory at all: an engine that reserves the whole GPU up front and
+ * hands out memory only from its own arena, a plugin living in a process
+ * whose allocator it does not own, or a latency-critical path that cannot
+ * afford cudaMalloc's implicit synchronisation. This entry point computes
+ * exactly what mla_tree_verify computes, with the same arguments minus
+ * workspace/workspace_bytes; its scratch lives in a fixed array of
+ * MT_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library keeps until the process exits. It never allocates.
+ *   - A request whose scratch (mla_tree_verify_workspace_bytes for the same
+ *     batch, total_q, heads, max_splits) exceeds MT_NOALLOC_SCRATCH_BYTES is
+ *     rejected with MT_ESCRATCH before anything is launched.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it needs clearing). Calls that may overlap on the
+ *     GPU -- unordered streams -- race on it; order them.
+ */
+#define MT_NOALLOC_SCRATCH_BYTES (64u << 20)
+int mla_tree_verify_noalloc(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                            const int32_t* kv_indices, int64_t kv_indices_len,
+                            const int32_t* kv_indptr, const int32_t* qo_indptr,
+                            const uint8_t* packed_mask, int64_t mask_len, const int64_t* mask_indptr,
+                            int batch, int total_q, int heads, float sm_scale,
+                            mt_bf16* out, float* lse, int max_splits, int path,
+                            int32_t* dev_status, mt_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,9 @@ PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 
 EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_scatter",
            "mla_tree_kv_indices_build", "tree_mask_pack", "mla_tree_verify_workspace_bytes",
-           "mla_tree_verify_launch_count", "mla_tree_verify"]
+           "mla_tree_verify_launch_count", "mla_tree_verify", "mla_tree_verify_noalloc"]
+MT_ESCRATCH = -5
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 P = ctypes.c_void_p
@@ -53,6 +55,9 @@ def load():
     lib.mla_tree_verify.restype = I32
     lib.mla_tree_verify.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                     P, P, P, SZ, I32, I32, P, P]
+    lib.mla_tree_verify_noalloc.restype = I32
+    lib.mla_tree_verify_noalloc.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
+                                            P, P, I32, I32, P, P]
     _lib = lib
     return lib
 
@@ -146,3 +151,23 @@ def mla_tree_verify(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, ma
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, path,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "mla_tree_verify")
+
+
+def mla_tree_verify_noalloc(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, mask_indptr,
+                            sm_scale, out, lse, max_splits=0, path=PATH_AUTO, status=None,
+                            stream=None):
+    """mla_tree_verify for callers that cannot allocate: the split scratch is
+    the library's built-in static device buffer instead of a workspace."""
+    if q.dim() != 3 or q.shape[2] != 576:
+        raise MlaTreeError("q must be [total_q, heads, 576]")
+    total_q, heads = q.shape[0], q.shape[1]
+    batch = qo_indptr.numel() - 1
+    rc = load().mla_tree_verify_noalloc(
+        _ptr(q, torch.bfloat16, "q"), _ptr(kv_buf, torch.bfloat16, "kv_buf"), kv_buf.shape[0],
+        _ptr(kv_indices, torch.int32, "kv_indices"), kv_indices.numel(),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(packed_mask, torch.uint8, "packed_mask"), packed_mask.numel(),
+        _ptr(mask_indptr, torch.int64, "mask_indptr"), batch, total_q, heads, float(sm_scale),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), max_splits, path,
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "mla_tree_verify_noalloc")

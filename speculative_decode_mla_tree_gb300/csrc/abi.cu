@@ -70,6 +70,7 @@ const char* mla_tree_status_string(int status) {
     case MT_EUNSUPPORTED: return "unsupported request";
     case MT_EWORKSPACE: return "workspace missing, misaligned or too small";
     case MT_ECUDA: return "CUDA error";
+    case MT_ESCRATCH: return "request needs more scratch than the built-in no-allocation buffer";
     default: return "unknown status";
   }
 }

@@ -15,7 +15,7 @@ from speculative_decode_mla_tree_gb300.step import VerifyStep
 from parity import OracleRun, bits, compare_attention, sample_rows
 
 pytestmark = pytest.mark.gpu
-PATHS = [pytest.param(abi.PATH_SIMT, id="simt"), pytest.param(abi.PATH_TC, id="tc")]
+PATHS = [pytest.param(abi.PATH_SIMT, id="simt"), pytest.param(abi.PATH_TC, id="tcgen05")]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -166,14 +166,18 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
 
 // ---------------------------------------------------------------- merge
 
-// One warp per (token, head) row, lane l owns output dims [16 l, 16 l + 16):
+// One 128-thread CTA per (token, head) row; thread t owns output dims
+// [4 t, 4 t + 4) and reads each split's 16 bytes of them independently, so
+// all splits of a row are in flight at once:
 //   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
 // Requests that ran unsplit (ws_nsplit[b] == 1) were finished in place.
-__global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const VerifyArgs a) {
-  const int lane = threadIdx.x & 31;
+constexpr int kMergeThreads = kDv / 4;
+constexpr int kMergeRegSplits = 16;  // splits merged with all loads in flight at once
+
+__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyArgs a) {
+  const int t4 = threadIdx.x;
   const int64_t R = (int64_t)a.total_q * a.heads;
-  const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (row >= R) return;
+  const int64_t row = blockIdx.x;
   const int64_t t = row / a.heads;
   const int b = find_request(a.qo_indptr, a.batch, t);
   const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
@@ -181,46 +185,62 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const VerifyArgs
   if (!g.ok || t < g.q0 || t >= g.q0 + g.n) return;
   const int S = a.ws_nsplit[b];
   if (S <= 1 || S > a.max_splits) return;
-  float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, a.ws_lse[(int64_t)s * R + row]);
-  float acc[16];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float tot = 0.f, mx = -INFINITY;
+  const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * kDv) + t4;
+  const int64_t step = R * (kDv / 4);  // float4s between consecutive splits of one row
+  if (S <= kMergeRegSplits) {
+    // every split's LSE and partial in flight at once, straight into registers
+    float ls[kMergeRegSplits];
+    float4 v[kMergeRegSplits];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-  float tot = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = a.ws_lse[(int64_t)s * R + row];
-      if (ls == -INFINITY) continue;
-      const float w = exp2f((ls - mx) * kLog2e);
-      tot += w;
-      const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((int64_t)s * R + row) * kDv) + 4 * lane;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 v = src[e];
-        acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
-        acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
-        acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
-        acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
+    for (int s = 0; s < kMergeRegSplits; ++s) {
+      if (s < S) {
+        ls[s] = __ldg(a.ws_lse + (int64_t)s * R + row);
+        v[s] = __ldg(src + (int64_t)s * step);
       }
+    }
+#pragma unroll
+    for (int s = 0; s < kMergeRegSplits; ++s)
+      if (s < S) mx = fmaxf(mx, ls[s]);
+#pragma unroll
+    for (int s = 0; s < kMergeRegSplits; ++s) {
+      if (s < S && mx != -INFINITY && ls[s] != -INFINITY) {
+        const float w = exp2f((ls[s] - mx) * kLog2e);
+        tot += w;
+        acc.x = fmaf(w, v[s].x, acc.x);
+        acc.y = fmaf(w, v[s].y, acc.y);
+        acc.z = fmaf(w, v[s].z, acc.z);
+        acc.w = fmaf(w, v[s].w, acc.w);
+      }
+    }
+  } else {
+    for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(a.ws_lse + (int64_t)s * R + row));
+    for (int s = 0; s < S && mx != -INFINITY; ++s) {
+      const float l2 = __ldg(a.ws_lse + (int64_t)s * R + row);
+      if (l2 == -INFINITY) continue;
+      const float w = exp2f((l2 - mx) * kLog2e);
+      const float4 x = __ldg(src + (int64_t)s * step);
+      tot += w;
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
     }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  uint32_t w[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-    w[e] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv) + 2 * lane;
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  if (lane == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 w2;
+  w2.x = *reinterpret_cast<const uint32_t*>(&lo);
+  w2.y = *reinterpret_cast<const uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(a.out + row * kDv)[t4] = w2;
+  if (t4 == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
   const int64_t R = (int64_t)a.total_q * a.heads;
-  const int64_t blocks = (R + kWarps - 1) / kWarps;
-  lse_merge_kernel<<<(unsigned)blocks, kWarps * 32, 0, stream>>>(a);
+  lse_merge_kernel<<<(unsigned)R, kMergeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

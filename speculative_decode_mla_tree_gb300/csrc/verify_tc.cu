@@ -57,6 +57,7 @@ constexpr int kThreads = 192;
 constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
+constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kQLat = 0;                              // 4 x [128 rows x 128 B], 128B swizzle
@@ -65,14 +66,15 @@ constexpr int kKV = kQRope + BM * 64;                 // key stages
 constexpr int kKVLat = BN * 128;                      // one latent chunk of a stage
 constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 36864
 constexpr int kStages = 2;
-constexpr int kP = kKV + kStages * kKVStage;          // P [128 x 64] bf16, 128B swizzle
-constexpr int kX = kP + BM * BN * 2;                  // exchange [128 x 64] fp32
+constexpr int kX = kKV + kStages * kKVStage;          // 2 x exchange [128 x 64] fp32
+constexpr int kXBytes = BM * BN * 4;
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
-constexpr int kVis = kX + BM * BN * 4;                // 2 x kVisNodes x 64-bit masks
+constexpr int kVis = kX + 2 * kXBytes;                // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
 enum {
   B_Q_FULL, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_EMPTY0, B_KV_EMPTY1, B_S_FULL0, B_S_FULL1,
-  B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_O_DONE, B_O_FREE, B_X_FULL, B_X_FREE, B_DRAIN, kNumBars
+  B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_O_DONE, B_O_FREE, B_X_FULL0, B_X_FULL1, B_X_FREE0,
+  B_X_FREE1, B_DRAIN, kNumBars
 };
 constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count
 constexpr int kPlan = kMisc + 32;                     // per-request plan
@@ -80,7 +82,7 @@ constexpr int kPlanStride = 10;                       // int32 words per request
 constexpr int kSmemUsed = kPlan + (kMaxBatch + 1) * kPlanStride * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kP % 1024 == 0 && kX % 1024 == 0 &&
+static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
                   kKVStage % 1024 == 0 && kBars % 8 == 0,
               "alignment");
 
@@ -89,6 +91,7 @@ constexpr uint32_t kKVTx = kKVStage;                  // key bytes per CTA per b
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;                        // 256 columns: O half
 constexpr uint32_t kTmemS = 256;                      // 2 x 64 columns: score buffers
+constexpr uint32_t kTmemP = 384;                      // 32 columns: P (bf16 pairs), PV's A
 constexpr uint64_t kDrainNs = 100000000ull;           // 100 ms
 
 // plan words
@@ -225,8 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_P_FULL], 128);
     mbar_init(&bars[B_O_DONE], 1);
     mbar_init(&bars[B_O_FREE], 128);
-    mbar_init(&bars[B_X_FULL], 128);
-    mbar_init(&bars[B_X_FREE], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[B_X_FULL0 + x], 1);  // own expect_tx arrival + the peer's bytes
+      mbar_init(&bars[B_X_FREE0 + x], 1);  // one elected arrival from the peer
+    }
     mbar_init(&bars[B_DRAIN], 1);
     *abort = 0;
     fence_mbar_init_cluster();
@@ -245,7 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before anyone arrives on them remotely
+  // The peer's barriers must exist before anyone touches them remotely: every
+  // thread arrives here, and only the softmax warps (the only ones that
+  // reach into the peer) wait before their first remote access.
+  cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   const int total_items = *total_items_s;
 
@@ -253,6 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t kb = 0, qi = 0;
     const int oob = (int)a.num_slots;  // an out-of-range row: TMA fills zeros
+    // slots of the four key rows lane l (< 16) gathers in block blk of an item
+    auto load_rows = [&](const Item& it, int blk, int (&rows)[4]) {
+      const int pos0 = it.j0 + blk * BN + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int slot = oob;
+        if (pos0 + e < it.j1) {
+          const int v = __ldg(a.kv_indices + it.kv0 + pos0 + e);
+          if (v >= 0 && v < a.num_slots) slot = v;
+          else flag(a.status, MT_DEV_BAD_SLOT);
+        }
+        rows[e] = slot;
+      }
+    };
     for (int id = cluster_id; id < total_items; id += p.nclusters) {
       const Item it = decode_item(plan, a.batch, id);
       const int qrow = it.q0 * H + it.row0;
@@ -265,6 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sm + kQRope, &tm_qrope, 512 + 32 * (int)cta, qrow, &bars[B_Q_FULL]);
       }
       ++qi;
+      int next_rows[4] = {oob, oob, oob, oob};
+      if (lane < 16) load_rows(it, 0, next_rows);
       for (int blk = 0; blk < it.nblocks; ++blk, ++kb) {
         const int s = kb & 1;
         uint8_t* st = sm + kKV + s * kKVStage;
@@ -274,24 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane < 16) {
-          const int pos0 = it.j0 + blk * BN + 4 * lane;
-          int rows[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            int slot = oob;
-            if (pos0 + e < it.j1) {
-              const int v = __ldg(a.kv_indices + it.kv0 + pos0 + e);
-              if (v >= 0 && v < a.num_slots) slot = v;
-              else flag(a.status, MT_DEV_BAD_SLOT);
-            }
-            rows[e] = slot;
-          }
+          const int rows[4] = {next_rows[0], next_rows[1], next_rows[2], next_rows[3]};
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tma_gather4(st + k * kKVLat + lane * 512, &tm_kvlat, 256 * (int)cta + 64 * k, rows[0],
                         rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
           tma_gather4(st + 4 * kKVLat + lane * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
                       rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
+          // the next block's slots load while this block's rows are in flight
+          if (blk + 1 < it.nblocks) load_rows(it, blk + 1, next_rows);
         }
         __syncwarp();
       }
@@ -308,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, 256, 0, 1);
       const uint32_t qlat = smem_u32(sm + kQLat), qrope = smem_u32(sm + kQRope);
-      const uint32_t pbuf = smem_u32(sm + kP), kvbase = smem_u32(sm + kKV);
+      const uint32_t kvbase = smem_u32(sm + kKV);
       for (int id = cluster_id; id < total_items; id += p.nclusters) {
         const Item it = decode_item(plan, a.batch, id);
         mbar_wait<false>(&bars[B_Q_FULL], qi & 1, abort);
@@ -348,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t stg = kvbase + s * kKVStage;
 #pragma unroll
           for (int t = 0; t < 4; ++t)
-            mma_bf16_ss(tmem + kTmemO, smem_desc(pbuf + 32 * t, 16, 1024, kSwizzle128B),
+            mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * t,
                         smem_desc(stg + t * 2048, 8192, 1024, kSwizzle128B), idesc_pv,
                         (blk | t) != 0);
           mma_commit(&bars[B_KV_EMPTY0 + s]);
@@ -363,17 +378,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax, exchange, epilogue
+    // Exchange: buffer X[g & 1] receives the peer's partial scores of block
+    // g (two buffers, so the peer may already send block g+1 while this CTA
+    // is still on block g); our own partial stays in TMEM until it is summed.
     const int r = tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO;
+    const uint32_t t_p = tmem + lane_base + kTmemP;
     const float scale2 = a.sm_scale * kLog2e;
-    float* X = reinterpret_cast<float*>(sm + kX);
-    const uint32_t x_peer = mapa(smem_u32(X + r * BN), peer);
-    const uint32_t xfull_peer = mapa(smem_u32(&bars[B_X_FULL]), peer);
-    const uint32_t xfree_peer = mapa(smem_u32(&bars[B_X_FREE]), peer);
-    uint8_t* prow = sm + kP + r * 128;
+    float* X0 = reinterpret_cast<float*>(sm + kX);
+    const uint32_t x_peer0 = mapa(smem_u32(X0 + r * BN), peer);
+    const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
+    const uint32_t xfree_peer0 = mapa(smem_u32(&bars[B_X_FREE0]), peer);
     const int64_t R = (int64_t)a.total_q * H;
-    uint32_t sc = 0, xc = 0, pw = 0, gblk = 0;
+    uint32_t pw = 0, gblk = 0;
+    cluster_wait();  // the peer's barriers are initialised
+
+    // Send this CTA's partial scores of global block g to the peer.
+    auto send = [&](uint32_t g) {
+      const uint32_t sb = g & 1, xb = g & 1;
+      mbar_wait<false>(&bars[B_S_FULL0 + sb], (g >> 1) & 1, abort);
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
+      tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
+      // arm our own receive buffer for the peer's block g (32 KB of bytes)
+      if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + xb], (uint32_t)kXBytes);
+      mbar_wait<true>(&bars[B_X_FREE0 + xb], ((g >> 1) & 1) ^ 1, abort);
+      const uint32_t dst = x_peer0 + xb * kXBytes;
+      const uint32_t bar = xfull_peer0 + 8 * xb;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(dst + ((c ^ (r & 15)) << 4), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2],
+                    s0[4 * c + 3], bar);
+#pragma unroll
+      for (int c = 8; c < 16; ++c)
+        st_async_v4(dst + ((c ^ (r & 15)) << 4), s1[4 * c - 32], s1[4 * c - 31], s1[4 * c - 30],
+                    s1[4 * c - 29], bar);
+    };
+    // Give buffer X[g & 1] back to the peer once all 128 rows have read it.
+    auto release_x = [&](uint32_t g) {
+      named_bar_sync(2, 128);
+      if (r == 0) mbar_arrive_remote(xfree_peer0 + 8 * (g & 1));
+    };
+
     for (int id = cluster_id; id < total_items; id += p.nclusters) {
       const Item it = decode_item(plan, a.batch, id);
       const int rows_req = it.n * H;
@@ -383,49 +431,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i_hi = min(it.n - 1, (it.row0 + BM - 1) / H);
       const int cnt = i_hi - i_lo + 1;
       const int node = (valid ? row : rows_req - 1) / H;
+      // Mask bytes of a block arrive as (draft node, 8-column group) pairs;
+      // thread r owns pairs r + 128 k. When a tile touches few enough nodes
+      // (every case with 8 or more heads), the bytes of block blk+1 are
+      // loaded while block blk is processed.
+      const int pairs = cnt * 8;
+      const bool prefetch = pairs <= 128 * kMaskPrefetch;
+      uint8_t raw[kMaskPrefetch][8];
+      auto load_mask = [&](int blk_) {
+        const int jb_ = it.j0 + blk_ * BN;
+#pragma unroll
+        for (int k = 0; k < kMaskPrefetch; ++k) {
+          const int q = r + 128 * k;
+          if (q < pairs) {
+            const int pos0 = jb_ + 8 * (q & 7);
+            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + (q >> 3)) * it.L + pos0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) raw[k][e] = pos0 + e < it.j1 ? __ldg(src + e) : 0;
+          }
+        }
+      };
+      if (prefetch) load_mask(0);
       float m = -INFINITY, l = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++gblk) {
+        send(gblk);
         const int jb = it.j0 + blk * BN;
         // visibility bits of this block for the tile's draft nodes
         uint8_t* vb = reinterpret_cast<uint8_t*>(vis + (gblk & 1) * kVisNodes);
-        for (int q = r; q < cnt * 8; q += 128) {
-          const int nl = q >> 3, g = q & 7;
-          const int pos0 = jb + 8 * g;
-          const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + nl) * it.L + pos0;
-          uint32_t bits = 0;
+        if (prefetch) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (pos0 + e < it.j1 && __ldg(src + e)) bits |= 1u << e;
-          vb[nl * 8 + g] = (uint8_t)bits;
+          for (int k = 0; k < kMaskPrefetch; ++k) {
+            const int q = r + 128 * k;
+            if (q < pairs) {
+              uint32_t bits = 0;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
+              vb[q] = (uint8_t)bits;
+            }
+          }
+          if (blk + 1 < it.nblocks) load_mask(blk + 1);
+        } else {
+          for (int q = r; q < pairs; q += 128) {
+            const int pos0 = jb + 8 * (q & 7);
+            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + (q >> 3)) * it.L + pos0;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (pos0 + e < it.j1 && __ldg(src + e)) bits |= 1u << e;
+            vb[q] = (uint8_t)bits;
+          }
         }
         named_bar_sync(1, 128);
         const uint64_t vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
 
-        // this CTA's partial scores
-        const uint32_t sb = sc & 1;
-        mbar_wait<false>(&bars[B_S_FULL0 + sb], (sc >> 1) & 1, abort);
-        tc_fence_after();
+        // full scores: the peer's partial (X) plus ours (still in TMEM)
+        const uint32_t xb = gblk & 1, sb = gblk & 1;
+        mbar_wait<true>(&bars[B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
         uint32_t s0[32], s1[32];
         tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
         tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
         tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY0 + sb]);
-        ++sc;
-
-        // exchange with the peer: send ours, receive theirs
-        mbar_wait<true>(&bars[B_X_FREE], (xc & 1) ^ 1, abort);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_cluster_v4(x_peer + ((c ^ (r & 15)) << 4), __uint_as_float(s0[4 * c]),
-                        __uint_as_float(s0[4 * c + 1]), __uint_as_float(s0[4 * c + 2]),
-                        __uint_as_float(s0[4 * c + 3]));
-#pragma unroll
-        for (int c = 8; c < 16; ++c)
-          st_cluster_v4(x_peer + ((c ^ (r & 15)) << 4), __uint_as_float(s1[4 * c - 32]),
-                        __uint_as_float(s1[4 * c - 31]), __uint_as_float(s1[4 * c - 30]),
-                        __uint_as_float(s1[4 * c - 29]));
-        mbar_arrive_remote(xfull_peer);
-        mbar_wait<true>(&bars[B_X_FULL], xc & 1, abort);
+        mbar_arrive(&bars[B_S_EMPTY0 + sb]);  // the score buffer may take block g+2
+        const float* X = X0 + xb * (kXBytes / 4);
         float s[64];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -436,21 +503,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[4 * c + 2] = __uint_as_float(own[2]) + v.z;
           s[4 * c + 3] = __uint_as_float(own[3]) + v.w;
         }
-        mbar_arrive_remote(xfree_peer);
-        ++xc;
+        // the last block's buffer stays ours: the epilogue stages rows in it
+        if (blk + 1 < it.nblocks) release_x(gblk);
 
         // masked online softmax (log2 domain)
+        const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
         float mb = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float v = ((vm >> c) & 1ull) ? s[c] * scale2 : -INFINITY;
+          const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
+          const float v = bit ? s[c] * scale2 : -INFINITY;
           s[c] = v;
           mb = fmaxf(mb, v);
         }
         float corr = 1.f;
         bool resc = false;
         if (mb > m + kRescale) {
-          corr = exp2f(m - mb);
+          corr = ex2_approx(m - mb);
           m = mb;
           resc = true;
         }
@@ -462,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = exp2f(s[2 * c] - m), p1 = exp2f(s[2 * c + 1] - m);
+            const float p0 = ex2_approx(s[2 * c] - m), p1 = ex2_approx(s[2 * c + 1] - m);
             const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
             // the denominator sums the same bf16 weights the P.V product uses,
             // so O / l stays a true weighted average of the value rows
@@ -472,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l = l * corr + rs;
 
-        // the previous P.V is done: P buffer and O may be touched
+        // the previous P.V is done: P and O may be touched
         if (blk > 0) {
           mbar_wait<false>(&bars[B_O_DONE], pw & 1, abort);
           ++pw;
@@ -489,59 +558,93 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
             tmem_st32(t_o + 32 * k, o);
           }
-          tmem_st_wait();
         }
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(prow + ((g ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-        fence_proxy_async_smem();
+        tmem_st32(t_p, pk);  // row r of P: 64 bf16 weights as 32 packed columns
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_P_FULL]);
       }
+      const uint32_t glast = gblk - 1;
 
-      // epilogue: O / l for this CTA's 256 value dims
+      // epilogue: O / l for this CTA's 256 value dims. Each 128-byte piece of
+      // every row goes through the last block's exchange buffer (still held),
+      // so a warp stores four whole 128-byte row pieces per instruction
+      // instead of 32 scattered 16-byte pieces.
       mbar_wait<false>(&bars[B_O_DONE], pw & 1, abort);
       ++pw;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t grow = (int64_t)it.q0 * H + row;
+      const int64_t row_base = (int64_t)it.q0 * H + it.row0;
+      const int valid_rows = min(BM, rows_req - it.row0);
+      uint8_t* stage = sm + kX + (glast & 1) * kXBytes;
+      named_bar_sync(3, 128);  // every row has read the last block's scores
+      if (it.splits == 1) {
 #pragma unroll 1
-      for (int k = 0; k < 8; ++k) {
-        uint32_t o[32];
-        tmem_ld32(t_o + 32 * k, o);
-        if (valid) {
-          if (it.splits == 1) {
-            uint32_t w[16];
+        for (int k = 0; k < 4; ++k) {  // 64 bf16 columns per round
+          uint32_t o0[32], o1[32];
+          tmem_ld32(t_o + 64 * k, o0);
+          tmem_ld32(t_o + 64 * k + 32, o1);
+          uint32_t w[32];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                             __uint_as_float(o[2 * e + 1]) * inv);
-              w[e] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.out + grow * kDv + 256 * cta + 32 * k);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(
-                a.ws_o + ((int64_t)it.split * R + grow) * kDv + 256 * cta + 32 * k);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                   __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(o0[2 * e]) * inv,
+                                                            __uint_as_float(o0[2 * e + 1]) * inv);
+            const __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(o1[2 * e]) * inv,
+                                                            __uint_as_float(o1[2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<const uint32_t*>(&v0);
+            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v1);
           }
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          named_bar_sync(3, 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int idx = i * 128 + r, rl = idx >> 3, g = idx & 7;
+            if (rl < valid_rows)
+              *reinterpret_cast<uint4*>(a.out + (row_base + rl) * kDv + 256 * cta + 64 * k + 8 * g) =
+                  *reinterpret_cast<const uint4*>(stage + rl * 128 + ((g ^ (rl & 7)) << 4));
+          }
+          named_bar_sync(3, 128);
+        }
+      } else {
+        float* wso = a.ws_o + ((int64_t)it.split * R + row_base) * kDv + 256 * cta;
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {  // 32 fp32 columns per round
+          uint32_t o[32];
+          tmem_ld32(t_o + 32 * k, o);
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) = make_uint4(
+                __float_as_uint(__uint_as_float(o[4 * g]) * inv),
+                __float_as_uint(__uint_as_float(o[4 * g + 1]) * inv),
+                __float_as_uint(__uint_as_float(o[4 * g + 2]) * inv),
+                __float_as_uint(__uint_as_float(o[4 * g + 3]) * inv));
+          named_bar_sync(3, 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int idx = i * 128 + r, rl = idx >> 3, g = idx & 7;
+            if (rl < valid_rows)
+              *reinterpret_cast<uint4*>(wso + (int64_t)rl * kDv + 32 * k + 4 * g) =
+                  *reinterpret_cast<const uint4*>(stage + rl * 128 + ((g ^ (rl & 7)) << 4));
+          }
+          named_bar_sync(3, 128);
         }
       }
       if (valid && cta == 0) {
         const float lv = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        const int64_t grow = row_base + r;
         if (it.splits == 1) a.lse[grow] = lv;
         else a.ws_lse[(int64_t)it.split * R + grow] = lv;
       }
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE]);
+      release_x(glast);  // staging done: the peer may refill this buffer
     }
   }
 
+  if (warp >= 4) cluster_wait();  // pairs with the arrival after set-up
   if (tid == 0 && *abort) flag(a.status, MT_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();

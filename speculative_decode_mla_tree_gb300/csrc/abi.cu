@@ -39,8 +39,8 @@ WorkspaceLayout workspace_layout(int batch, int total_q, int heads, int max_spli
   WorkspaceLayout w;
   const size_t rows = (size_t)total_q * (size_t)heads;
   size_t off = 0;
-  w.nsplit_off = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)(batch > 0 ? batch : 1), 256);
+  w.tok_off = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1), 256);
   w.lse_off = off;
   off = align_up(off + sizeof(float) * (size_t)max_splits * rows, 256);
   w.o_off = off;
@@ -180,9 +180,10 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
   a.out = out;
   a.lse = lse;
   a.max_splits = max_splits;
+  a.partial_f16 = 0;
   a.status = dev_status;
   char* ws = (char*)workspace;
-  a.ws_nsplit = (int32_t*)(ws + wl.nsplit_off);
+  a.ws_tok = (int32_t*)(ws + wl.tok_off);
   a.ws_lse = (float*)(ws + wl.lse_off);
   a.ws_o = (float*)(ws + wl.o_off);
   a.ws_counter = (int32_t*)(ws + wl.counter_off);

@@ -23,9 +23,11 @@ struct VerifyArgs {
   uint16_t* out;                // bf16 [total_q, heads, 512]
   float* lse;                   // fp32 [total_q, heads]
   int max_splits;               // capacity of the partial buffers
+  int partial_f16;              // split partials stored as fp16 (else fp32)
   int32_t* status;
   // workspace views
-  int32_t* ws_nsplit;           // [batch] split count each request used
+  int32_t* ws_tok;              // [total_q] split count of each token's request (0: not
+                                //   merged: unsplit, empty or inconsistent request)
   float* ws_lse;                // [max_splits][total_q*heads]
   float* ws_o;                  // [max_splits][total_q*heads][512]
   int32_t* ws_counter;          // [tiles] arrival counters (tensor-core path)
@@ -33,7 +35,7 @@ struct VerifyArgs {
 };
 
 struct WorkspaceLayout {
-  size_t nsplit_off, lse_off, o_off, counter_off, total;
+  size_t tok_off, lse_off, o_off, counter_off, total;
   int64_t counter_len;
 };
 

@@ -14,6 +14,7 @@
 // (the 512 latent dims the lane already holds). Scores are reduced with xor
 // shuffles, so every lane holds the same bits; the online softmax runs in
 // the log2 domain with sm_scale * log2(e) folded into q.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "mt_common.cuh"
@@ -59,12 +60,15 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
                                  a.mask_len, a.total_q);
   if (!g.ok || t < g.q0 || t >= g.q0 + g.n) {
-    if (lane == 0 && split == 0) flag(a.status, MT_DEV_BAD_INDPTR);
+    if (lane == 0 && split == 0) {
+      flag(a.status, MT_DEV_BAD_INDPTR);
+      if (h0 == 0) a.ws_tok[t] = 0;  // nothing to merge for this token
+    }
     return;
   }
   int chunk;
   const int S = simt_splits(g.L, a.max_splits, &chunk);
-  if (split == 0 && lane == 0 && t == g.q0 && h0 == 0) a.ws_nsplit[b] = S;
+  if (split == 0 && lane == 0 && h0 == 0) a.ws_tok[t] = S;
   if (split >= S) return;
   const int j0 = split * chunk;
   const int j1 = min(g.L, j0 + chunk);
@@ -166,45 +170,57 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
 
 // ---------------------------------------------------------------- merge
 
-// One 128-thread CTA per (token, head) row; thread t owns output dims
-// [4 t, 4 t + 4) and reads each split's 16 bytes of them independently, so
-// all splits of a row are in flight at once:
+// One CTA per (token, group of kMergeHeads heads); thread (h, d) owns output
+// dims [4 d, 4 d + 4) of head h of the group:
 //   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
-// Requests that ran unsplit (ws_nsplit[b] == 1) were finished in place.
-constexpr int kMergeThreads = kDv / 4;
-constexpr int kMergeRegSplits = 16;  // splits merged with all loads in flight at once
+// The producing kernel records each token's split count, so one load decides
+// the work; then every split's LSE and partial are loaded at once (up to
+// kMergeRegSplits splits): two dependent memory rounds per row. Tokens of
+// unsplit requests were finished in place.
+// Partials are fp32 (warp-shuffle path) or fp16 (tensor-core path).
+constexpr int kMergeHeads = 1;
+constexpr int kMergeThreads = kMergeHeads * (kDv / 4);
+constexpr int kMergeRegSplits = 12;
 
+__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __half* p) {
+  const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+  const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+template <typename P>
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyArgs a) {
-  const int t4 = threadIdx.x;
-  const int64_t R = (int64_t)a.total_q * a.heads;
-  const int64_t row = blockIdx.x;
-  const int64_t t = row / a.heads;
-  const int b = find_request(a.qo_indptr, a.batch, t);
-  const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
-                                 a.mask_len, a.total_q);
-  if (!g.ok || t < g.q0 || t >= g.q0 + g.n) return;
-  const int S = a.ws_nsplit[b];
+  const int tid = threadIdx.x;
+  const int hl = tid / (kDv / 4), d4 = tid % (kDv / 4);
+  const int64_t t = blockIdx.x;
+  // split count of the token's request, recorded by the producing kernel
+  // (0 or 1: nothing to merge)
+  const int S = __ldg(a.ws_tok + t);
   if (S <= 1 || S > a.max_splits) return;
+  const int h = blockIdx.y * kMergeHeads + hl;
+  if (S == 0 || h >= a.heads) return;
+  const int64_t R = (int64_t)a.total_q * a.heads;
+  const int64_t row = t * a.heads + h;
+  const P* base = reinterpret_cast<const P*>(a.ws_o) + row * kDv + 4 * d4;
+  const int64_t step = R * kDv;  // elements between two splits of one row
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float tot = 0.f, mx = -INFINITY;
-  const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * kDv) + t4;
-  const int64_t step = R * (kDv / 4);  // float4s between consecutive splits of one row
   if (S <= kMergeRegSplits) {
-    // every split's LSE and partial in flight at once, straight into registers
     float ls[kMergeRegSplits];
     float4 v[kMergeRegSplits];
 #pragma unroll
-    for (int s = 0; s < kMergeRegSplits; ++s) {
+    for (int s = 0; s < kMergeRegSplits; ++s)
       if (s < S) {
         ls[s] = __ldg(a.ws_lse + (int64_t)s * R + row);
-        v[s] = __ldg(src + (int64_t)s * step);
+        v[s] = load4(base + (int64_t)s * step);
       }
-    }
 #pragma unroll
     for (int s = 0; s < kMergeRegSplits; ++s)
       if (s < S) mx = fmaxf(mx, ls[s]);
 #pragma unroll
-    for (int s = 0; s < kMergeRegSplits; ++s) {
+    for (int s = 0; s < kMergeRegSplits; ++s)
       if (s < S && mx != -INFINITY && ls[s] != -INFINITY) {
         const float w = exp2f((ls[s] - mx) * kLog2e);
         tot += w;
@@ -213,14 +229,13 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
         acc.z = fmaf(w, v[s].z, acc.z);
         acc.w = fmaf(w, v[s].w, acc.w);
       }
-    }
   } else {
     for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(a.ws_lse + (int64_t)s * R + row));
     for (int s = 0; s < S && mx != -INFINITY; ++s) {
       const float l2 = __ldg(a.ws_lse + (int64_t)s * R + row);
       if (l2 == -INFINITY) continue;
       const float w = exp2f((l2 - mx) * kLog2e);
-      const float4 x = __ldg(src + (int64_t)s * step);
+      const float4 x = load4(base + (int64_t)s * step);
       tot += w;
       acc.x = fmaf(w, x.x, acc.x);
       acc.y = fmaf(w, x.y, acc.y);
@@ -234,13 +249,16 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
   uint2 w2;
   w2.x = *reinterpret_cast<const uint32_t*>(&lo);
   w2.y = *reinterpret_cast<const uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(a.out + row * kDv)[t4] = w2;
-  if (t4 == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  reinterpret_cast<uint2*>(a.out + row * kDv)[d4] = w2;
+  if (d4 == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
-  const int64_t R = (int64_t)a.total_q * a.heads;
-  lse_merge_kernel<<<(unsigned)R, kMergeThreads, 0, stream>>>(a);
+  dim3 grid((unsigned)a.total_q, (unsigned)((a.heads + kMergeHeads - 1) / kMergeHeads));
+  if (a.partial_f16)
+    lse_merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(a);
+  else
+    lse_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,8 @@
 
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "mt_common.cuh"
 #include "mt_internal.h"
 #include "sm100_ptx.cuh"
@@ -52,7 +54,8 @@ namespace tc {
 using namespace sm100;
 
 constexpr int BM = 128;          // tile rows = TMEM lanes
-constexpr int BN = 64;           // key rows per block
+constexpr int BN = 48;           // key rows per block
+constexpr int kGatherLanes = BN / 4;  // producer lanes, four rows each (tile::gather4)
 constexpr int kThreads = 192;
 constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
@@ -64,15 +67,17 @@ constexpr int kQLat = 0;                              // 4 x [128 rows x 128 B],
 constexpr int kQRope = kQLat + 4 * BM * 128;          // [128 rows x 64 B], 64B swizzle
 constexpr int kKV = kQRope + BM * 64;                 // key stages
 constexpr int kKVLat = BN * 128;                      // one latent chunk of a stage
-constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 36864
-constexpr int kStages = 2;
-constexpr int kX = kKV + kStages * kKVStage;          // 2 x exchange [128 x 64] fp32
-constexpr int kXBytes = BM * BN * 4;
+constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 27648
+constexpr int kStages = 3;
+constexpr int kX = kKV + kStages * kKVStage;          // 2 x exchange [128 rows x BN] fp32
+constexpr int kXRow = BN * 4 + 16;                    // padded row: rows land on different banks
+constexpr int kXBytes = BM * kXRow;
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
 constexpr int kVis = kX + 2 * kXBytes;                // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
 enum {
-  B_Q_FULL, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_EMPTY0, B_KV_EMPTY1, B_S_FULL0, B_S_FULL1,
+  B_Q_FULL, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_FULL2, B_KV_EMPTY0, B_KV_EMPTY1, B_KV_EMPTY2,
+  B_S_FULL0, B_S_FULL1,
   B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_O_DONE, B_O_FREE, B_X_FULL0, B_X_FULL1, B_X_FREE0,
   B_X_FREE1, B_DRAIN, kNumBars
 };
@@ -82,6 +87,8 @@ constexpr int kPlanStride = 10;                       // int32 words per request
 constexpr int kSmemUsed = kPlan + (kMaxBatch + 1) * kPlanStride * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kXBytes >= BM * 128, "epilogue staging fits in one exchange buffer");
+static_assert(BN % 16 == 0 && BN <= 64, "block width");
 static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
                   kKVStage % 1024 == 0 && kBars % 8 == 0,
               "alignment");
@@ -91,7 +98,7 @@ constexpr uint32_t kKVTx = kKVStage;                  // key bytes per CTA per b
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;                        // 256 columns: O half
 constexpr uint32_t kTmemS = 256;                      // 2 x 64 columns: score buffers
-constexpr uint32_t kTmemP = 384;                      // 32 columns: P (bf16 pairs), PV's A
+constexpr uint32_t kTmemP = 384;                      // BN/2 columns: P (bf16 pairs), PV's A
 constexpr uint64_t kDrainNs = 100000000ull;           // 100 ms
 
 // plan words
@@ -181,7 +188,10 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* t
       items = tiles * S;
       pr[PL_SPLITS] = S;
       pr[PL_LEN] = len;
-      if (publish) a.ws_nsplit[b] = S;
+      if (publish) {  // every token of this request: its split count for the merge
+        const int q0 = pr[PL_Q0], n = tiles > 0 ? pr[PL_N] : 0;
+        for (int tk = 0; tk < n; ++tk) a.ws_tok[q0 + tk] = S;
+      }
     }
     int incl = items;
 #pragma unroll
@@ -191,6 +201,18 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* t
     }
     if (b < a.batch) plan[b * kPlanStride + PL_BASE] = carry + incl - items;
     carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  // tokens of inconsistent requests (or outside every request) are not merged
+  if (publish) {
+    __syncwarp();
+    for (int tk = lane; tk < a.total_q; tk += 32) {
+      int covered = 0;
+      for (int b = 0; b < a.batch && !covered; ++b) {
+        const int* pr = plan + b * kPlanStride;
+        covered = pr[PL_TILES] > 0 && tk >= pr[PL_Q0] && tk < pr[PL_Q0] + pr[PL_N];
+      }
+      if (!covered) a.ws_tok[tk] = 0;
+    }
   }
   if (lane == 0) *total_items = carry;
 }
@@ -219,9 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[B_KV_FULL0 + s], 1);
       mbar_init(&bars[B_KV_EMPTY0 + s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[B_S_FULL0 + s], 1);
       mbar_init(&bars[B_S_EMPTY0 + s], 128);
     }
@@ -288,16 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++qi;
       int next_rows[4] = {oob, oob, oob, oob};
-      if (lane < 16) load_rows(it, 0, next_rows);
+      if (lane < kGatherLanes) load_rows(it, 0, next_rows);
       for (int blk = 0; blk < it.nblocks; ++blk, ++kb) {
-        const int s = kb & 1;
+        const int s = kb % kStages;
         uint8_t* st = sm + kKV + s * kKVStage;
         if (lane == 0) {
-          mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb >> 1) & 1) ^ 1, abort);
+          mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort);
           mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
         }
         __syncwarp();
-        if (lane < 16) {
+        if (lane < kGatherLanes) {
           const int rows[4] = {next_rows[0], next_rows[1], next_rows[2], next_rows[3]};
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -313,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {  // every copy this CTA issued has landed before it may exit
       if (qi > 0) mbar_drain(&bars[B_Q_FULL], (qi - 1) & 1, kDrainNs);
-      for (uint32_t k = kb >= 2 ? kb - 2 : 0; k < kb; ++k)
-        mbar_drain(&bars[B_KV_FULL0 + (k & 1)], (k >> 1) & 1, kDrainNs);
+      for (uint32_t k = kb >= kStages ? kb - kStages : 0; k < kb; ++k)
+        mbar_drain(&bars[B_KV_FULL0 + (k % kStages)], (k / kStages) & 1, kDrainNs);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -334,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // scores of block blk+1 go first so they overlap the softmax of block blk
           if (blk + 1 < it.nblocks) {
             const uint32_t kbi = kb0 + blk + 1;
-            const uint32_t s = kbi & 1, sb = sc & 1;
-            mbar_wait<false>(&bars[B_KV_FULL0 + s], (kbi >> 1) & 1, abort);
+            const uint32_t s = kbi % kStages, sb = sc & 1;
+            mbar_wait<false>(&bars[B_KV_FULL0 + s], (kbi / kStages) & 1, abort);
             mbar_wait<false>(&bars[B_S_EMPTY0 + sb], ((sc >> 1) & 1) ^ 1, abort);
             tc_fence_after();
             const uint32_t stg = kvbase + s * kKVStage;
@@ -359,12 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (blk == 0) mbar_wait<false>(&bars[B_O_FREE], (ii & 1) ^ 1, abort);
           mbar_wait<false>(&bars[B_P_FULL], pc & 1, abort);
           tc_fence_after();
-          const uint32_t s = (kb0 + blk) & 1;
+          const uint32_t s = (kb0 + blk) % kStages;
           const uint32_t stg = kvbase + s * kKVStage;
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
+          for (int t = 0; t < BN / 16; ++t)
             mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * t,
-                        smem_desc(stg + t * 2048, 8192, 1024, kSwizzle128B), idesc_pv,
+                        smem_desc(stg + t * 2048, kKVLat, 1024, kSwizzle128B), idesc_pv,
                         (blk | t) != 0);
           mma_commit(&bars[B_KV_EMPTY0 + s]);
           mma_commit(&bars[B_O_DONE]);
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_p = tmem + lane_base + kTmemP;
     const float scale2 = a.sm_scale * kLog2e;
     float* X0 = reinterpret_cast<float*>(sm + kX);
-    const uint32_t x_peer0 = mapa(smem_u32(X0 + r * BN), peer);
+    const uint32_t x_peer0 = mapa(smem_u32(sm + kX + r * kXRow), peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
     const uint32_t xfree_peer0 = mapa(smem_u32(&bars[B_X_FREE0]), peer);
     const int64_t R = (int64_t)a.total_q * H;
@@ -399,27 +423,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sb = g & 1, xb = g & 1;
       mbar_wait<false>(&bars[B_S_FULL0 + sb], (g >> 1) & 1, abort);
       tc_fence_after();
-      uint32_t s0[32], s1[32];
+      uint32_t s0[32], s1[16];
       tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
-      tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
+      tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
       // arm our own receive buffer for the peer's block g (32 KB of bytes)
-      if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + xb], (uint32_t)kXBytes);
+      if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + xb], (uint32_t)(BM * BN * 4));  // bytes sent, not padded
       mbar_wait<true>(&bars[B_X_FREE0 + xb], ((g >> 1) & 1) ^ 1, abort);
       const uint32_t dst = x_peer0 + xb * kXBytes;
       const uint32_t bar = xfull_peer0 + 8 * xb;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        st_async_v4(dst + ((c ^ (r & 15)) << 4), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2],
-                    s0[4 * c + 3], bar);
+        st_async_v4(dst + (c << 4), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2], s0[4 * c + 3], bar);
 #pragma unroll
-      for (int c = 8; c < 16; ++c)
-        st_async_v4(dst + ((c ^ (r & 15)) << 4), s1[4 * c - 32], s1[4 * c - 31], s1[4 * c - 30],
+      for (int c = 8; c < BN / 4; ++c)
+        st_async_v4(dst + (c << 4), s1[4 * c - 32], s1[4 * c - 31], s1[4 * c - 30],
                     s1[4 * c - 29], bar);
     };
     // Give buffer X[g & 1] back to the peer once all 128 rows have read it.
+    // Every row's reads are complete here (their values were consumed before
+    // the barrier), so the signal needs no release fence; a release would make
+    // the signalling thread wait for its own outstanding st.async sends.
     auto release_x = [&](uint32_t g) {
       named_bar_sync(2, 128);
-      if (r == 0) mbar_arrive_remote(xfree_peer0 + 8 * (g & 1));
+      if (r == 0) mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
     };
 
     for (int id = cluster_id; id < total_items; id += p.nclusters) {
@@ -435,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // thread r owns pairs r + 128 k. When a tile touches few enough nodes
       // (every case with 8 or more heads), the bytes of block blk+1 are
       // loaded while block blk is processed.
-      const int pairs = cnt * 8;
+      constexpr int kGroups = BN / 8;  // 8-column groups per block row
+      const int pairs = cnt * kGroups;
       const bool prefetch = pairs <= 128 * kMaskPrefetch;
       uint8_t raw[kMaskPrefetch][8];
       auto load_mask = [&](int blk_) {
@@ -444,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kMaskPrefetch; ++k) {
           const int q = r + 128 * k;
           if (q < pairs) {
-            const int pos0 = jb_ + 8 * (q & 7);
-            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + (q >> 3)) * it.L + pos0;
+            const int pos0 = jb_ + 8 * (q % kGroups);
+            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
 #pragma unroll
             for (int e = 0; e < 8; ++e) raw[k][e] = pos0 + e < it.j1 ? __ldg(src + e) : 0;
           }
@@ -454,6 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (prefetch) load_mask(0);
       float m = -INFINITY, l = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++gblk) {
+        // Sending block blk+1 ahead of block blk's softmax was measured
+        // slower: the swap then competes with the key gathers for the SM's
+        // inbound bandwidth while the softmax waits on both.
         send(gblk);
         const int jb = it.j0 + blk * BN;
         // visibility bits of this block for the tile's draft nodes
@@ -466,19 +496,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t bits = 0;
 #pragma unroll
               for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
-              vb[q] = (uint8_t)bits;
+              vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
             }
           }
           if (blk + 1 < it.nblocks) load_mask(blk + 1);
         } else {
           for (int q = r; q < pairs; q += 128) {
-            const int pos0 = jb + 8 * (q & 7);
-            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + (q >> 3)) * it.L + pos0;
+            const int pos0 = jb + 8 * (q % kGroups);
+            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
             uint32_t bits = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               if (pos0 + e < it.j1 && __ldg(src + e)) bits |= 1u << e;
-            vb[q] = (uint8_t)bits;
+            vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
           }
         }
         named_bar_sync(1, 128);
@@ -487,16 +517,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // full scores: the peer's partial (X) plus ours (still in TMEM)
         const uint32_t xb = gblk & 1, sb = gblk & 1;
         mbar_wait<true>(&bars[B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
-        uint32_t s0[32], s1[32];
+        uint32_t s0[32], s1[16];
         tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
-        tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
+        tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
         tc_fence_before();
         mbar_arrive(&bars[B_S_EMPTY0 + sb]);  // the score buffer may take block g+2
-        const float* X = X0 + xb * (kXBytes / 4);
-        float s[64];
+        const float* X = reinterpret_cast<const float*>(sm + kX + xb * kXBytes + r * kXRow);
+        float s[BN];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = *reinterpret_cast<const float4*>(X + r * BN + ((c ^ (r & 15)) << 2));
+        for (int c = 0; c < BN / 4; ++c) {
+          const float4 v = *reinterpret_cast<const float4*>(X + 4 * c);
           const uint32_t* own = c < 8 ? &s0[4 * c] : &s1[4 * c - 32];
           s[4 * c] = __uint_as_float(own[0]) + v.x;
           s[4 * c + 1] = __uint_as_float(own[1]) + v.y;
@@ -510,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
         float mb = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < BN; ++c) {
           const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
           const float v = bit ? s[c] * scale2 : -INFINITY;
           s[c] = v;
@@ -525,12 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float rs = 0.f;
         uint32_t pk[32];
+#pragma unroll
+        for (int c = BN / 2; c < 32; ++c) pk[c] = 0u;  // columns past the block are not read
         if (m == -INFINITY) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+          for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < BN / 2; ++c) {
             const float p0 = ex2_approx(s[2 * c] - m), p1 = ex2_approx(s[2 * c + 1] - m);
             const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
             // the denominator sums the same bf16 weights the P.V product uses,
@@ -609,24 +641,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(3, 128);
         }
       } else {
-        float* wso = a.ws_o + ((int64_t)it.split * R + row_base) * kDv + 256 * cta;
+        // split partials in fp16 (each is a convex combination of value rows;
+        // 11 significand bits keep it far below the bf16 output rounding)
+        __half* wso = reinterpret_cast<__half*>(a.ws_o) + ((int64_t)it.split * R + row_base) * kDv + 256 * cta;
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {  // 32 fp32 columns per round
-          uint32_t o[32];
-          tmem_ld32(t_o + 32 * k, o);
+        for (int k = 0; k < 4; ++k) {  // 64 columns per round
+          uint32_t o0[32], o1[32];
+          tmem_ld32(t_o + 64 * k, o0);
+          tmem_ld32(t_o + 64 * k + 32, o1);
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __half2 v0 = __floats2half2_rn(__uint_as_float(o0[2 * e]) * inv,
+                                                 __uint_as_float(o0[2 * e + 1]) * inv);
+            const __half2 v1 = __floats2half2_rn(__uint_as_float(o1[2 * e]) * inv,
+                                                 __uint_as_float(o1[2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<const uint32_t*>(&v0);
+            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v1);
+          }
 #pragma unroll
           for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) = make_uint4(
-                __float_as_uint(__uint_as_float(o[4 * g]) * inv),
-                __float_as_uint(__uint_as_float(o[4 * g + 1]) * inv),
-                __float_as_uint(__uint_as_float(o[4 * g + 2]) * inv),
-                __float_as_uint(__uint_as_float(o[4 * g + 3]) * inv));
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
           named_bar_sync(3, 128);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int idx = i * 128 + r, rl = idx >> 3, g = idx & 7;
             if (rl < valid_rows)
-              *reinterpret_cast<uint4*>(wso + (int64_t)rl * kDv + 32 * k + 4 * g) =
+              *reinterpret_cast<uint4*>(wso + (int64_t)rl * kDv + 64 * k + 8 * g) =
                   *reinterpret_cast<const uint4*>(stage + rl * 128 + ((g ^ (rl & 7)) << 4));
           }
           named_bar_sync(3, 128);
@@ -733,6 +775,7 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
     return cudaErrorNotSupported;
   TcParams p;
   p.a = a;
+  p.a.partial_f16 = 1;
   p.nclusters = nclusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters);
@@ -748,7 +791,7 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, p, tq_lat, tq_rope, tkv_lat, tkv_rope);
   if (e != cudaSuccess) return e;
-  if (a.max_splits > 1) return launch_lse_merge(a, stream);
+  if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
   return cudaSuccess;
 }
 

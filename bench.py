@@ -356,7 +356,7 @@ def run_ours(args):
                        "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
                        "path": ["auto", "simt", "tensor-core"][args.path],
                        "max_splits": args.max_splits,
-                       "l2": "flushed between steps (256 MiB write outside the events)",
+                       "l2": "flushed between steps: 256 MiB written then read back, outside the events",
                        "timing": "per-call CUDA graphs, CUDA events on the launching stream"},
             "step_ms": {"scatter": statistics.mean(call_ms[0]), "kv_indices": statistics.mean(call_ms[1]),
                         "mask_pack": statistics.mean(call_ms[2]), "verify": verify_ms,

@@ -195,9 +195,13 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
   const int tid = threadIdx.x;
   const int hl = tid / (kDv / 4), d4 = tid % (kDv / 4);
   const int64_t t = blockIdx.x;
+  // When launched as a dependent grid of the producing kernel, wait for it
+  // to complete (and its writes to be visible) before reading anything it
+  // wrote; otherwise this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // split count of the token's request, recorded by the producing kernel
   // (0 or 1: nothing to merge)
-  const int S = __ldg(a.ws_tok + t);
+  const int S = __ldcg(a.ws_tok + t);
   if (S <= 1 || S > a.max_splits) return;
   const int h = blockIdx.y * kMergeHeads + hl;
   if (S == 0 || h >= a.heads) return;
@@ -254,12 +258,20 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
 }
 
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
-  dim3 grid((unsigned)a.total_q, (unsigned)((a.heads + kMergeHeads - 1) / kMergeHeads));
-  if (a.partial_f16)
-    lse_merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(a);
-  else
-    lse_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the merge grid is scheduled while the
+  // producing kernel drains and waits on-device for its completion, which
+  // hides the launch gap between the two.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.total_q, (unsigned)((a.heads + kMergeHeads - 1) / kMergeHeads));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (a.partial_f16) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__half>, a);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<float>, a);
 }
 
 }  // namespace mt

@@ -31,8 +31,9 @@
 // shared memory. Splitting the dims halves both, leaves TMEM room for two S
 // buffers, and keeps the exchange to the 64-column score block.
 //
-// Roles per CTA (192 threads): warps 0-3 softmax / exchange / epilogue (one
-// thread per TMEM lane = tile row), warp 4 TMA producer, warp 5 MMA issuer
+// Roles per CTA (288 threads): warps 0-3 softmax / exchange / epilogue (one
+// thread per TMEM lane = tile row), warps 4-7 TMA producers (one warp alone
+// issues tile::gather4 too slowly to keep up), warp 8 MMA issuer
 // and TMEM owner. Every mbarrier wait is time-bounded: a timeout sets
 // MT_DEV_TIMEOUT, after which the CTA runs through to its exit without
 // waiting, draining its asynchronous copies and MMAs before releasing TMEM.
@@ -55,8 +56,10 @@ using namespace sm100;
 
 constexpr int BM = 128;          // tile rows = TMEM lanes
 constexpr int BN = 48;           // key rows per block
-constexpr int kGatherLanes = BN / 4;  // producer lanes, four rows each (tile::gather4)
-constexpr int kThreads = 192;
+constexpr int kGatherLanes = BN / 4;  // four-row groups per block (tile::gather4)
+constexpr int kProducers = 4;    // TMA producer warps (one warp issues about 37 ns per gather4)
+constexpr int kThreads = 32 * (4 + kProducers + 1);
+constexpr int kMmaWarp = 4 + kProducers;
 constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
@@ -83,8 +86,10 @@ enum {
 };
 constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count
 constexpr int kPlan = kMisc + 32;                     // per-request plan
-constexpr int kPlanStride = 10;                       // int32 words per request
-constexpr int kSmemUsed = kPlan + (kMaxBatch + 1) * kPlanStride * 4;
+constexpr int kPlanStride = 9;                        // int32 words per request
+constexpr int kOrd = kPlan + kMaxBatch * kPlanStride * 4;   // request at each rank
+constexpr int kOBase = kOrd + kMaxBatch * 4;          // first item of each rank (+ total)
+constexpr int kSmemUsed = kOBase + (kMaxBatch + 1) * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kXBytes >= BM * 128, "epilogue staging fits in one exchange buffer");
@@ -102,7 +107,7 @@ constexpr uint32_t kTmemP = 384;                      // BN/2 columns: P (bf16 p
 constexpr uint64_t kDrainNs = 100000000ull;           // 100 ms
 
 // plan words
-enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_BASE, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI };
+enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI };
 
 struct TcParams {
   VerifyArgs a;
@@ -115,22 +120,34 @@ struct Item {
   int64_t mask0;
 };
 
-__device__ __forceinline__ Item decode_item(const int* plan, int batch, int id) {
-  int lo = 0, hi = batch - 1;  // last request whose first item is <= id
+// Item numbering: requests are ranked (longest split first when the items
+// take more than one round of the persistent grid), a request's items are
+// numbered tile-major, and cluster c takes item k * nclusters + c in even
+// rounds k and k * nclusters + (nclusters - 1 - c) in odd ones, so the
+// longest items are spread over the clusters first and every cluster's
+// total comes out close to the mean.
+__device__ __forceinline__ int item_of(int k, int c, int nclusters) {
+  return k * nclusters + ((k & 1) ? nclusters - 1 - c : c);
+}
+
+__device__ __forceinline__ Item decode_item(const int* plan, const int* ord, const int* obase,
+                                            int batch, int id) {
+  int lo = 0, hi = batch - 1;  // last rank whose first item is <= id
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (plan[mid * kPlanStride + PL_BASE] <= id) lo = mid; else hi = mid - 1;
+    if (obase[mid] <= id) lo = mid; else hi = mid - 1;
   }
-  const int* pr = plan + lo * kPlanStride;
+  const int b = ord[lo];
+  const int* pr = plan + b * kPlanStride;
   Item it;
-  it.b = lo;
+  it.b = b;
   it.q0 = pr[PL_Q0];
   it.n = pr[PL_N];
   it.kv0 = pr[PL_KV0];
   it.L = pr[PL_L];
   it.splits = pr[PL_SPLITS];
   const int len = pr[PL_LEN];
-  const int local = id - pr[PL_BASE];
+  const int local = id - obase[lo];
   it.tile = local / it.splits;
   it.split = local - it.tile * it.splits;
   it.j0 = it.split * len;
@@ -141,11 +158,21 @@ __device__ __forceinline__ Item decode_item(const int* plan, int batch, int id) 
   return it;
 }
 
+__device__ __forceinline__ long long warp_sum(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Warp 0: per-request geometry, split counts and the item numbering. Every
 // CTA computes the same plan from the device indptrs; CTA 0 also publishes
 // the split counts for the merge kernel.
-__device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* total_items,
-                           int lane, bool publish) {
+//
+// Split length: a quarter of one cluster's fair share of (tile x key) work,
+// at least kMinChunk keys, so that a long request is cut into enough items
+// for every cluster to get several and the last round stays short.
+__device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* ord, int* obase,
+                           int* total_items, int lane, bool publish) {
   const int H = a.heads;
   long long units = 0;
   for (int b = lane; b < a.batch; b += 32) {
@@ -164,34 +191,59 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* t
     pr[PL_M0HI] = (int)(g.mask0 >> 32);
     units += (long long)tiles * g.L;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
-  long long chunk = (units + nclusters - 1) / (nclusters > 0 ? nclusters : 1);
+  units = warp_sum(units);
+  const long long nc = nclusters > 0 ? nclusters : 1;
+  long long chunk = (units + 4 * nc - 1) / (4 * nc);
   if (chunk < kMinChunk) chunk = kMinChunk;
   chunk = (chunk + BN - 1) / BN * BN;
+  long long items_total = 0;
+  for (int b = lane; b < a.batch; b += 32) {
+    int* pr = plan + b * kPlanStride;
+    const int tiles = pr[PL_TILES];
+    const int L = pr[PL_L];
+    int S = 1, len = BN;
+    if (tiles > 0 && L > 0) {
+      long long s = (L + chunk - 1) / chunk;
+      if (s > a.max_splits) s = a.max_splits;
+      if (s < 1) s = 1;
+      len = (int)(((L + s - 1) / s + BN - 1) / BN * BN);
+      S = (L + len - 1) / len;
+    }
+    pr[PL_SPLITS] = S;
+    pr[PL_LEN] = len;
+    items_total += (long long)tiles * S;
+    if (publish) {  // every token of this request: its split count for the merge
+      const int q0 = pr[PL_Q0], n = tiles > 0 ? pr[PL_N] : 0;
+      for (int tk = 0; tk < n; ++tk) a.ws_tok[q0 + tk] = S;
+    }
+  }
+  items_total = warp_sum(items_total);
+  __syncwarp();
+  // rank the requests: by split length, longest first, when the items take
+  // more than one round; else in request order
+  const bool sorted = items_total > nc;
+  for (int b = lane; b < a.batch; b += 32) {
+    int rank = b;
+    if (sorted) {
+      const int* pb = plan + b * kPlanStride;
+      const int key = pb[PL_TILES] > 0 ? pb[PL_LEN] : -1;
+      rank = 0;
+      for (int o = 0; o < a.batch; ++o) {
+        const int* po = plan + o * kPlanStride;
+        const int ko = po[PL_TILES] > 0 ? po[PL_LEN] : -1;
+        rank += (ko > key) || (ko == key && o < b);
+      }
+    }
+    ord[rank] = b;
+  }
+  __syncwarp();
   int carry = 0;
   for (int base = 0; base < a.batch; base += 32) {
-    const int b = base + lane;
+    const int r = base + lane;
     int items = 0;
-    if (b < a.batch) {
-      int* pr = plan + b * kPlanStride;
-      const int tiles = pr[PL_TILES];
-      const int L = pr[PL_L];
-      int S = 1, len = BN;
-      if (tiles > 0 && L > 0) {
-        long long s = (L + chunk - 1) / chunk;
-        if (s > a.max_splits) s = a.max_splits;
-        if (s < 1) s = 1;
-        len = (int)(((L + s - 1) / s + BN - 1) / BN * BN);
-        S = (L + len - 1) / len;
-      }
-      items = tiles * S;
-      pr[PL_SPLITS] = S;
-      pr[PL_LEN] = len;
-      if (publish) {  // every token of this request: its split count for the merge
-        const int q0 = pr[PL_Q0], n = tiles > 0 ? pr[PL_N] : 0;
-        for (int tk = 0; tk < n; ++tk) a.ws_tok[q0 + tk] = S;
-      }
+    if (r < a.batch) {
+      const int* pr = plan + ord[r] * kPlanStride;
+      items = pr[PL_TILES] * pr[PL_SPLITS];
     }
     int incl = items;
 #pragma unroll
@@ -199,7 +251,7 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* t
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    if (b < a.batch) plan[b * kPlanStride + PL_BASE] = carry + incl - items;
+    if (r < a.batch) obase[r] = carry + incl - items;
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   // tokens of inconsistent requests (or outside every request) are not merged
@@ -214,7 +266,10 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* t
       if (!covered) a.ws_tok[tk] = 0;
     }
   }
-  if (lane == 0) *total_items = carry;
+  if (lane == 0) {
+    obase[a.batch] = carry;
+    *total_items = carry;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -236,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kMisc + 4);
   int* total_items_s = reinterpret_cast<int*>(sm + kMisc + 8);
   int* plan = reinterpret_cast<int*>(sm + kPlan);
+  int* ord = reinterpret_cast<int*>(sm + kOrd);
+  int* obase = reinterpret_cast<int*>(sm + kOBase);
   uint64_t* vis = reinterpret_cast<uint64_t*>(sm + kVis);
 
   if (tid == 0) {
@@ -260,17 +317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort = 0;
     fence_mbar_init_cluster();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 4 && lane == 0) {  // first producer warp
     prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qrope);
     prefetch_tmap(&tm_kvlat);
     prefetch_tmap(&tm_kvrope);
   }
-  if (warp == 0) build_plan(a, p.nclusters, plan, total_items_s, lane, blockIdx.x == 0);
+  if (warp == 0) build_plan(a, p.nclusters, plan, ord, obase, total_items_s, lane, blockIdx.x == 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -281,13 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int total_items = *total_items_s;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp >= 4 && warp < 4 + kProducers) {
+    // ------------------------------------------------------------ producers
+    // kProducers warps share every block's gathers: warp pw issues the
+    // four-row groups [pw * kGroupsPerWarp, (pw + 1) * kGroupsPerWarp), one
+    // group per lane. The first producer warp also loads the query tile and
+    // arms each stage's barrier with the whole stage's byte count (bytes of
+    // the other warps may land before that arrival; the phase cannot
+    // complete without it).
+    constexpr int kGroupsPerWarp = kGatherLanes / kProducers;
+    static_assert(kGatherLanes % kProducers == 0, "groups per producer warp");
+    const int pw = warp - 4;
+    const int grp = pw * kGroupsPerWarp + lane;
+    const bool gathers = lane < kGroupsPerWarp;
     uint32_t kb = 0, qi = 0;
     const int oob = (int)a.num_slots;  // an out-of-range row: TMA fills zeros
-    // slots of the four key rows lane l (< 16) gathers in block blk of an item
+    // slots of the four key rows of this lane's group in block blk of an item
     auto load_rows = [&](const Item& it, int blk, int (&rows)[4]) {
-      const int pos0 = it.j0 + blk * BN + 4 * lane;
+      const int pos0 = it.j0 + blk * BN + 4 * grp;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         int slot = oob;
@@ -299,10 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows[e] = slot;
       }
     };
-    for (int id = cluster_id; id < total_items; id += p.nclusters) {
-      const Item it = decode_item(plan, a.batch, id);
+    for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
+         id = item_of(++rnd, cluster_id, p.nclusters)) {
+      const Item it = decode_item(plan, ord, obase, a.batch, id);
       const int qrow = it.q0 * H + it.row0;
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort);
         mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTx);
         for (int k = 0; k < 4; ++k)
@@ -312,22 +381,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++qi;
       int next_rows[4] = {oob, oob, oob, oob};
-      if (lane < kGatherLanes) load_rows(it, 0, next_rows);
+      if (gathers) load_rows(it, 0, next_rows);
       for (int blk = 0; blk < it.nblocks; ++blk, ++kb) {
         const int s = kb % kStages;
         uint8_t* st = sm + kKV + s * kKVStage;
         if (lane == 0) {
           mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort);
-          mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
+          if (pw == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
         }
         __syncwarp();
-        if (lane < kGatherLanes) {
+        if (gathers) {
           const int rows[4] = {next_rows[0], next_rows[1], next_rows[2], next_rows[3]};
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tma_gather4(st + k * kKVLat + lane * 512, &tm_kvlat, 256 * (int)cta + 64 * k, rows[0],
+            tma_gather4(st + k * kKVLat + grp * 512, &tm_kvlat, 256 * (int)cta + 64 * k, rows[0],
                         rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
-          tma_gather4(st + 4 * kKVLat + lane * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
+          tma_gather4(st + 4 * kKVLat + grp * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
                       rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
           // the next block's slots load while this block's rows are in flight
           if (blk + 1 < it.nblocks) load_rows(it, blk + 1, next_rows);
@@ -335,12 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
-    if (lane == 0) {  // every copy this CTA issued has landed before it may exit
+    if (pw == 0 && lane == 0) {  // every copy this CTA issued has landed before it may exit
       if (qi > 0) mbar_drain(&bars[B_Q_FULL], (qi - 1) & 1, kDrainNs);
       for (uint32_t k = kb >= kStages ? kb - kStages : 0; k < kb; ++k)
         mbar_drain(&bars[B_KV_FULL0 + (k % kStages)], (k / kStages) & 1, kDrainNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t kb = 0, sc = 0, pc = 0, qi = 0, ii = 0;
@@ -348,8 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = idesc_bf16(BM, 256, 0, 1);
       const uint32_t qlat = smem_u32(sm + kQLat), qrope = smem_u32(sm + kQRope);
       const uint32_t kvbase = smem_u32(sm + kKV);
-      for (int id = cluster_id; id < total_items; id += p.nclusters) {
-        const Item it = decode_item(plan, a.batch, id);
+      for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
+         id = item_of(++rnd, cluster_id, p.nclusters)) {
+        const Item it = decode_item(plan, ord, obase, a.batch, id);
         mbar_wait<false>(&bars[B_Q_FULL], qi & 1, abort);
         ++qi;
         tc_fence_after();
@@ -448,8 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r == 0) mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
     };
 
-    for (int id = cluster_id; id < total_items; id += p.nclusters) {
-      const Item it = decode_item(plan, a.batch, id);
+    for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
+         id = item_of(++rnd, cluster_id, p.nclusters)) {
+      const Item it = decode_item(plan, ord, obase, a.batch, id);
       const int rows_req = it.n * H;
       const int row = it.row0 + r;
       const bool valid = row < rows_req;
@@ -687,10 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp >= 4) cluster_wait();  // pairs with the arrival after set-up
+  // this CTA's outputs are issued: the merge kernel (launched as a dependent
+  // grid) may start its set-up; it waits for this grid's completion before
+  // reading any partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0 && *abort) flag(a.status, MT_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

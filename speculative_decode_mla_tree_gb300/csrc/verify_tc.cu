@@ -13,27 +13,29 @@
 // contiguous range of its key positions (a split). A tile is served by a
 // cluster of two CTAs on two SMs that split the head dims: CTA c holds
 // latent dims [256c, 256c+256) and rope dims [512+32c, 512+32c+32) of the
-// query tile and of every key row. Per block of 64 key rows:
+// query tile and of every key row. Per block of BN = 48 key rows:
 //
 //   TMA       the query half once per item (tile loads); key-row halves by
 //             tile::gather4 through kv_indices, four rows per instruction
-//   tcgen05   S_c = Q_c K_c^T   (M=128, N=64, K=288) into TMEM
-//   DSMEM     each CTA sends its partial S_c to its peer; both form
-//             S_0 + S_1 in the same order, so both hold bit-identical S
+//   tcgen05   S_c = Q_c K_c^T   (M=128, N=48, K=288) into TMEM
+//   DSMEM     each CTA rounds its partial S_c (scaled to the log2
+//             domain) to fp16 and sends it to its peer; both form
+//             fp16(S_0) + fp16(S_1) in fp32, so both hold bit-identical S
 //   softmax   mask bytes staged per block as bits, online max / sum in the
 //             log2 domain with lazy rescaling (the running max moves only
 //             when it grows by more than 8, i.e. a factor of 256)
-//   tcgen05   O_c += P V_c      (M=128, N=256, K=64) into TMEM; V_c is the
+//   tcgen05   O_c += P V_c      (M=128, N=256, K=48) into TMEM; V_c is the
 //             same shared-memory key tile, read MN-major
 //
 // Why two CTAs: a 128-row fp32 accumulator for all 512 value dims is the
 // whole 256 KB of TMEM, and a 128-row query tile of 576 dims is 144 KB of
 // shared memory. Splitting the dims halves both, leaves TMEM room for two S
-// buffers, and keeps the exchange to the 64-column score block.
+// buffers, and keeps the exchange to the 48-column score block.
 //
-// Roles per CTA (288 threads): warps 0-3 softmax / exchange / epilogue (one
-// thread per TMEM lane = tile row), warps 4-7 TMA producers (one warp alone
-// issues tile::gather4 too slowly to keep up), warp 8 MMA issuer
+// Roles per CTA (384 threads): warps 0-3 softmax / epilogue (one thread per
+// TMEM lane = tile row), warps 4-7 score senders (same lanes), warps 8-10
+// TMA producers (one warp alone issues tile::gather4 too slowly to keep
+// up), warp 11 MMA issuer
 // and TMEM owner. Every mbarrier wait is time-bounded: a timeout sets
 // MT_DEV_TIMEOUT, after which the CTA runs through to its exit without
 // waiting, draining its asynchronous copies and MMAs before releasing TMEM.
@@ -57,9 +59,10 @@ using namespace sm100;
 constexpr int BM = 128;          // tile rows = TMEM lanes
 constexpr int BN = 48;           // key rows per block
 constexpr int kGatherLanes = BN / 4;  // four-row groups per block (tile::gather4)
-constexpr int kProducers = 4;    // TMA producer warps (one warp issues about 37 ns per gather4)
-constexpr int kThreads = 32 * (4 + kProducers + 1);
-constexpr int kMmaWarp = 4 + kProducers;
+constexpr int kProducers = 3;    // TMA producer warps (one warp issues about 37 ns per gather4)
+constexpr int kFirstProducer = 8;  // warps 0-3 softmax, 4-7 score senders
+constexpr int kMmaWarp = kFirstProducer + kProducers;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
@@ -72,11 +75,11 @@ constexpr int kKV = kQRope + BM * 64;                 // key stages
 constexpr int kKVLat = BN * 128;                      // one latent chunk of a stage
 constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 27648
 constexpr int kStages = 3;
-constexpr int kX = kKV + kStages * kKVStage;          // 2 x exchange [128 rows x BN] fp32
-constexpr int kXRow = BN * 4 + 16;                    // padded row: rows land on different banks
-constexpr int kXBytes = BM * kXRow;
+constexpr int kX = kKV + kStages * kKVStage;          // exchange: [XO0 | XP0 | XO1 | XP1]
+constexpr int kXRow = BN * 2 + 16;                    // fp16 scores of one row, padded: rows land on different banks
+constexpr int kXBytes = BM * kXRow;                   // one buffer (own XO or peer's XP)
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
-constexpr int kVis = kX + 2 * kXBytes;                // 2 x kVisNodes x 64-bit masks
+constexpr int kVis = kX + 4 * kXBytes;                // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
 enum {
   B_Q_FULL, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_FULL2, B_KV_EMPTY0, B_KV_EMPTY1, B_KV_EMPTY2,
@@ -92,7 +95,7 @@ constexpr int kOBase = kOrd + kMaxBatch * 4;          // first item of each rank
 constexpr int kSmemUsed = kOBase + (kMaxBatch + 1) * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kXBytes >= BM * 128, "epilogue staging fits in one exchange buffer");
+static_assert(2 * kXBytes >= BM * 128, "epilogue staging fits in one XO/XP pair");
 static_assert(BN % 16 == 0 && BN <= 64, "block width");
 static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
                   kKVStage % 1024 == 0 && kBars % 8 == 0,
@@ -310,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_O_DONE], 1);
     mbar_init(&bars[B_O_FREE], 128);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[B_X_FULL0 + x], 1);  // own expect_tx arrival + the peer's bytes
-      mbar_init(&bars[B_X_FREE0 + x], 1);  // one elected arrival from the peer
+      mbar_init(&bars[B_X_FULL0 + x], 128);  // own senders (one with expect_tx) + the peer's bytes
+      mbar_init(&bars[B_X_FREE0 + x], 2);    // own softmax rows and the peer's, one elected arrival each
     }
     mbar_init(&bars[B_DRAIN], 1);
     *abort = 0;
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {  // first producer warp
+  if (warp == kFirstProducer && lane == 0) {
     prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qrope);
     prefetch_tmap(&tm_kvlat);
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int total_items = *total_items_s;
 
-  if (warp >= 4 && warp < 4 + kProducers) {
+  if (warp >= kFirstProducer && warp < kFirstProducer + kProducers) {
     // ------------------------------------------------------------ producers
     // kProducers warps share every block's gathers: warp pw issues the
     // four-row groups [pw * kGroupsPerWarp, (pw + 1) * kGroupsPerWarp), one
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // complete without it).
     constexpr int kGroupsPerWarp = kGatherLanes / kProducers;
     static_assert(kGatherLanes % kProducers == 0, "groups per producer warp");
-    const int pw = warp - 4;
+    const int pw = warp - kFirstProducer;
     const int grp = pw * kGroupsPerWarp + lane;
     const bool gathers = lane < kGroupsPerWarp;
     uint32_t kb = 0, qi = 0;
@@ -470,52 +473,87 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[B_DRAIN]);  // everything issued has completed before TMEM is freed
       mbar_drain(&bars[B_DRAIN], 0, kDrainNs);
     }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ score senders
+    // Thread r owns row r (TMEM lane r). As soon as the scores of a block are
+    // in TMEM it reads its row of this CTA's partial S_c = Q_c K_c^T, scales
+    // it into the log2 domain, rounds it to fp16 and writes it twice: into
+    // the own buffer XO and, by st.async, into the peer's buffer XP, whose
+    // arrival completes the peer's X_FULL. Both CTAs then form
+    // fp32(XO) + fp32(XP) with the same two fp16 terms, so they hold the
+    // same scores bit for bit. Working ahead of the softmax warps, the
+    // senders overlap a block's exchange with the previous block's softmax.
+    const int r = tid - 128;
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const float scale2 = a.sm_scale * kLog2e;
+    const uint32_t xp_peer0 = mapa(smem_u32(sm + kX + kXBytes + r * kXRow), peer);
+    const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
+    uint32_t g = 0;
+    cluster_wait();  // the peer's barriers are initialised
+    for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
+         id = item_of(++rnd, cluster_id, p.nclusters)) {
+      const Item it = decode_item(plan, ord, obase, a.batch, id);
+      for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
+        const uint32_t b = g & 1;
+        mbar_wait<false>(&bars[B_S_FULL0 + b], (g >> 1) & 1, abort);
+        tc_fence_after();
+        uint32_t s0[32], s1[16];
+        tmem_ld32(tmem + lane_base + kTmemS + 64 * b, s0);
+        tmem_ld16(tmem + lane_base + kTmemS + 64 * b + 32, s1);
+        tc_fence_before();
+        mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
+        uint32_t h[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+          // clamp to the finite fp16 range (scores that large saturate the
+          // softmax either way)
+          const float x0 = fminf(fmaxf(__uint_as_float(u0) * scale2, -65504.f), 65504.f);
+          const float x1 = fminf(fmaxf(__uint_as_float(u1) * scale2, -65504.f), 65504.f);
+          const __half2 v = __floats2half2_rn(x0, x1);
+          h[c] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        // both halves of buffer pair b are free: our softmax rows and the
+        // peer's have read block g-2
+        mbar_wait<true>(&bars[B_X_FREE0 + b], ((g >> 1) & 1) ^ 1, abort);
+        uint8_t* xo = sm + kX + 2 * b * kXBytes + r * kXRow;
+        const uint32_t dst = xp_peer0 + 2 * b * kXBytes;
+        const uint32_t bar = xfull_peer0 + 8 * b;
+#pragma unroll
+        for (int q = 0; q < BN / 8; ++q) {
+          *reinterpret_cast<uint4*>(xo + 16 * q) = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+          st_async_v4(dst + 16 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3], bar);
+        }
+        // own row written; r == 0 also arms the barrier for the peer's bytes
+        if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + b], (uint32_t)(BM * BN * 2));
+        else mbar_arrive(&bars[B_X_FULL0 + b]);
+      }
+    }
   } else {
-    // ------------------------------------------------------------ softmax, exchange, epilogue
-    // Exchange: buffer X[g & 1] receives the peer's partial scores of block
-    // g (two buffers, so the peer may already send block g+1 while this CTA
-    // is still on block g); our own partial stays in TMEM until it is summed.
+    // ------------------------------------------------------------ softmax, epilogue
+    // Block g's scores come from buffer pair g & 1 (XO: ours, XP: the
+    // peer's), two pairs so the senders may fill block g+1 while the rows
+    // are still on block g.
     const int r = tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO;
     const uint32_t t_p = tmem + lane_base + kTmemP;
-    const float scale2 = a.sm_scale * kLog2e;
-    float* X0 = reinterpret_cast<float*>(sm + kX);
-    const uint32_t x_peer0 = mapa(smem_u32(sm + kX + r * kXRow), peer);
-    const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
     const uint32_t xfree_peer0 = mapa(smem_u32(&bars[B_X_FREE0]), peer);
     const int64_t R = (int64_t)a.total_q * H;
     uint32_t pw = 0, gblk = 0;
     cluster_wait();  // the peer's barriers are initialised
 
-    // Send this CTA's partial scores of global block g to the peer.
-    auto send = [&](uint32_t g) {
-      const uint32_t sb = g & 1, xb = g & 1;
-      mbar_wait<false>(&bars[B_S_FULL0 + sb], (g >> 1) & 1, abort);
-      tc_fence_after();
-      uint32_t s0[32], s1[16];
-      tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
-      tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
-      // arm our own receive buffer for the peer's block g (32 KB of bytes)
-      if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + xb], (uint32_t)(BM * BN * 4));  // bytes sent, not padded
-      mbar_wait<true>(&bars[B_X_FREE0 + xb], ((g >> 1) & 1) ^ 1, abort);
-      const uint32_t dst = x_peer0 + xb * kXBytes;
-      const uint32_t bar = xfull_peer0 + 8 * xb;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(dst + (c << 4), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2], s0[4 * c + 3], bar);
-#pragma unroll
-      for (int c = 8; c < BN / 4; ++c)
-        st_async_v4(dst + (c << 4), s1[4 * c - 32], s1[4 * c - 31], s1[4 * c - 30],
-                    s1[4 * c - 29], bar);
-    };
-    // Give buffer X[g & 1] back to the peer once all 128 rows have read it.
-    // Every row's reads are complete here (their values were consumed before
-    // the barrier), so the signal needs no release fence; a release would make
-    // the signalling thread wait for its own outstanding st.async sends.
+    // Give buffer pair g & 1 back once all 128 rows have read it: to our own
+    // senders (XO) and to the peer's (our XP is theirs to fill). Every row's
+    // reads are complete here (their values were consumed before the
+    // barrier), so the remote signal needs no release fence.
     auto release_x = [&](uint32_t g) {
       named_bar_sync(2, 128);
-      if (r == 0) mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
+      if (r == 0) {
+        mbar_arrive(&bars[B_X_FREE0 + (g & 1)]);
+        mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
+      }
     };
 
     for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
@@ -552,10 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (prefetch) load_mask(0);
       float m = -INFINITY, l = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++gblk) {
-        // Sending block blk+1 ahead of block blk's softmax was measured
-        // slower: the swap then competes with the key gathers for the SM's
-        // inbound bandwidth while the softmax waits on both.
-        send(gblk);
         const int jb = it.j0 + blk * BN;
         // visibility bits of this block for the tile's draft nodes
         uint8_t* vb = reinterpret_cast<uint8_t*>(vis + (gblk & 1) * kVisNodes);
@@ -585,26 +619,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);
         const uint64_t vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
 
-        // full scores: the peer's partial (X) plus ours (still in TMEM)
-        const uint32_t xb = gblk & 1, sb = gblk & 1;
+        // full scores (log2 domain): our fp16 partial plus the peer's
+        const uint32_t xb = gblk & 1;
         mbar_wait<true>(&bars[B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
-        uint32_t s0[32], s1[16];
-        tmem_ld32(tmem + lane_base + kTmemS + 64 * sb, s0);
-        tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 32, s1);
-        tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY0 + sb]);  // the score buffer may take block g+2
-        const float* X = reinterpret_cast<const float*>(sm + kX + xb * kXBytes + r * kXRow);
+        const uint8_t* xo = sm + kX + 2 * xb * kXBytes + r * kXRow;
+        const uint8_t* xp = xo + kXBytes;
         float s[BN];
 #pragma unroll
-        for (int c = 0; c < BN / 4; ++c) {
-          const float4 v = *reinterpret_cast<const float4*>(X + 4 * c);
-          const uint32_t* own = c < 8 ? &s0[4 * c] : &s1[4 * c - 32];
-          s[4 * c] = __uint_as_float(own[0]) + v.x;
-          s[4 * c + 1] = __uint_as_float(own[1]) + v.y;
-          s[4 * c + 2] = __uint_as_float(own[2]) + v.z;
-          s[4 * c + 3] = __uint_as_float(own[3]) + v.w;
+        for (int q = 0; q < BN / 8; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(xo + 16 * q);
+          const uint4 v = *reinterpret_cast<const uint4*>(xp + 16 * q);
+          const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 fu = __half22float2(*reinterpret_cast<const __half2*>(&uu[e]));
+            const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&vv[e]));
+            s[8 * q + 2 * e] = fu.x + fv.x;
+            s[8 * q + 2 * e + 1] = fu.y + fv.y;
+          }
         }
-        // the last block's buffer stays ours: the epilogue stages rows in it
+        // the last block's pair stays ours: the epilogue stages rows in it
         if (blk + 1 < it.nblocks) release_x(gblk);
 
         // masked online softmax (log2 domain)
@@ -613,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
-          const float v = bit ? s[c] * scale2 : -INFINITY;
+          const float v = bit ? s[c] : -INFINITY;
           s[c] = v;
           mb = fmaxf(mb, v);
         }
@@ -679,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t row_base = (int64_t)it.q0 * H + it.row0;
       const int valid_rows = min(BM, rows_req - it.row0);
-      uint8_t* stage = sm + kX + (glast & 1) * kXBytes;
+      uint8_t* stage = sm + kX + 2 * (glast & 1) * kXBytes;
       named_bar_sync(3, 128);  // every row has read the last block's scores
       if (it.splits == 1) {
 #pragma unroll 1
@@ -757,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (warp >= 4) cluster_wait();  // pairs with the arrival after set-up
+  if (warp >= kFirstProducer) cluster_wait();  // pairs with the arrival after set-up
   // this CTA's outputs are issued: the merge kernel (launched as a dependent
   // grid) may start its set-up; it waits for this grid's completion before
   // reading any partial

@@ -15,8 +15,10 @@
 // latent dims [256c, 256c+256) and rope dims [512+32c, 512+32c+32) of the
 // query tile and of every key row. Per block of BN = 48 key rows:
 //
-//   TMA       the query half once per item (tile loads); key-row halves by
-//             tile::gather4 through kv_indices, four rows per instruction
+//   query     per item: the rope half by TMA into shared memory, the
+//             256 latent dims by the sender warps straight into TMEM
+//   TMA       key-row halves by tile::gather4 through kv_indices, four rows
+//             per instruction, five stages in flight
 //   tcgen05   S_c = Q_c K_c^T   (M=128, N=48, K=288) into TMEM
 //   DSMEM     each CTA rounds its partial S_c (scaled to the log2
 //             domain) to fp16 and sends it to its peer; both form
@@ -28,9 +30,10 @@
 //             same shared-memory key tile, read MN-major
 //
 // Why two CTAs: a 128-row fp32 accumulator for all 512 value dims is the
-// whole 256 KB of TMEM, and a 128-row query tile of 576 dims is 144 KB of
-// shared memory. Splitting the dims halves both, leaves TMEM room for two S
-// buffers, and keeps the exchange to the 48-column score block.
+// whole 256 KB of TMEM. Splitting the dims halves it and leaves TMEM room
+// for the query's latent half (so the QK MMAs read no query bytes from
+// shared memory, which at N = 48 would otherwise bound them) and two score
+// buffers; the exchange stays at the 48-column score block.
 //
 // Roles per CTA (384 threads): warps 0-3 softmax / epilogue (one thread per
 // TMEM lane = tile row), warps 4-7 score senders (same lanes), warps 8-10
@@ -67,26 +70,34 @@ constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
 constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
+constexpr int kSlotAhead = 4;    // key blocks whose slot numbers are in flight ahead of the gathers
 
 // Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kQLat = 0;                              // 4 x [128 rows x 128 B], 128B swizzle
-constexpr int kQRope = kQLat + 4 * BM * 128;          // [128 rows x 64 B], 64B swizzle
+constexpr int kQRope = 0;                             // query rope half [128 rows x 64 B], 64B swizzle
 constexpr int kKV = kQRope + BM * 64;                 // key stages
 constexpr int kKVLat = BN * 128;                      // one latent chunk of a stage
 constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 27648
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kX = kKV + kStages * kKVStage;          // exchange: [XO0 | XP0 | XO1 | XP1]
 constexpr int kXRow = BN * 2 + 16;                    // fp16 scores of one row, padded: rows land on different banks
 constexpr int kXBytes = BM * kXRow;                   // one buffer (own XO or peer's XP)
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
 constexpr int kVis = kX + 4 * kXBytes;                // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
-enum {
-  B_Q_FULL, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_FULL2, B_KV_EMPTY0, B_KV_EMPTY1, B_KV_EMPTY2,
-  B_S_FULL0, B_S_FULL1,
-  B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_O_DONE, B_O_FREE, B_X_FULL0, B_X_FULL1, B_X_FREE0,
-  B_X_FREE1, B_DRAIN, kNumBars
-};
+constexpr int B_Q_FULL = 0;                     // query rope half landed (TMA)
+constexpr int B_QT_FULL = 1;                    // query latent half written to TMEM
+constexpr int B_Q_EMPTY = 2;                    // last QK of the item done
+constexpr int B_KV_FULL0 = 3;                   // kStages barriers each
+constexpr int B_KV_EMPTY0 = B_KV_FULL0 + kStages;
+constexpr int B_S_FULL0 = B_KV_EMPTY0 + kStages;  // two each from here
+constexpr int B_S_EMPTY0 = B_S_FULL0 + 2;
+constexpr int B_X_FULL0 = B_S_EMPTY0 + 2;
+constexpr int B_X_FREE0 = B_X_FULL0 + 2;
+constexpr int B_P_FULL = B_X_FREE0 + 2;
+constexpr int B_O_DONE = B_P_FULL + 1;
+constexpr int B_O_FREE = B_O_DONE + 1;
+constexpr int B_DRAIN = B_O_FREE + 1;
+constexpr int kNumBars = B_DRAIN + 1;
 constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count
 constexpr int kPlan = kMisc + 32;                     // per-request plan
 constexpr int kPlanStride = 9;                        // int32 words per request
@@ -101,13 +112,23 @@ static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
                   kKVStage % 1024 == 0 && kBars % 8 == 0,
               "alignment");
 
-constexpr uint32_t kQTx = 4 * BM * 128 + BM * 64;     // query bytes per CTA per item
+constexpr uint32_t kQTx = BM * 64;                    // query rope bytes per CTA per item
 constexpr uint32_t kKVTx = kKVStage;                  // key bytes per CTA per block
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;                        // 256 columns: O half
-constexpr uint32_t kTmemS = 256;                      // 2 x 64 columns: score buffers
-constexpr uint32_t kTmemP = 384;                      // BN/2 columns: P (bf16 pairs), PV's A
+// TMEM columns (512 x 128 lanes; lane = tile row):
+//   [0, 256)    O, this CTA's 256 value dims (fp32)
+//   [256, 384)  Q, this CTA's 256 latent query dims as bf16 pairs: QK's A
+//               operand (no shared-memory reads of Q per MMA)
+//   [384, 432)  S buffer 0, [448, 496) S buffer 1 (BN fp32 scores each)
+//   P (bf16 pairs, PV's A), one 8-column piece per 16 keys, in the gaps:
+//   [432, 448) and [496, 504)
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemQ = 256;
+constexpr uint32_t kTmemS = 384;                      // buffer b at kTmemS + 64 b
+__host__ __device__ constexpr uint32_t tmem_p_col(int t) { return t < 2 ? 432u + 8u * t : 496u; }
+static_assert(BN == 48, "TMEM map holds 48-column score blocks and three P pieces");
 constexpr uint64_t kDrainNs = 100000000ull;           // 100 ms
+constexpr long long kIdleLimitCycles = 4000000000ll;  // about 2 s of SM clock with nothing to issue
 
 // plan words
 enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI };
@@ -276,7 +297,7 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    verify_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_qlat,
+    verify_tc_kernel(const __grid_constant__ TcParams p,
                      const __grid_constant__ CUtensorMap tm_qrope,
                      const __grid_constant__ CUtensorMap tm_kvlat,
                      const __grid_constant__ CUtensorMap tm_kvrope) {
@@ -300,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
+    mbar_init(&bars[B_QT_FULL], 128);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[B_KV_FULL0 + s], 1);
@@ -314,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_O_FREE], 128);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[B_X_FULL0 + x], 128);  // own senders (one with expect_tx) + the peer's bytes
-      mbar_init(&bars[B_X_FREE0 + x], 2);    // own softmax rows and the peer's, one elected arrival each
+      mbar_init(&bars[B_X_FREE0 + x], 8);    // own four softmax warps and the peer's, one arrival each
     }
     mbar_init(&bars[B_DRAIN], 1);
     *abort = 0;
@@ -325,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kFirstProducer && lane == 0) {
-    prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qrope);
     prefetch_tmap(&tm_kvlat);
     prefetch_tmap(&tm_kvrope);
@@ -356,14 +377,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool gathers = lane < kGroupsPerWarp;
     uint32_t kb = 0, qi = 0;
     const int oob = (int)a.num_slots;  // an out-of-range row: TMA fills zeros
-    // slots of the four key rows of this lane's group in block blk of an item
-    auto load_rows = [&](const Item& it, int blk, int (&rows)[4]) {
+    // Slots of the four key rows of this lane's group in block blk of an
+    // item: the loads are only issued here (bit e of `live` marks a position
+    // inside the split); the values are checked by take_rows when their
+    // gathers are issued, so the load latency stays hidden.
+    auto load_rows = [&](const Item& it, int blk, int (&rows)[4], int& live) {
       const int pos0 = it.j0 + blk * BN + 4 * grp;
+      live = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        rows[e] = oob;
+        if (pos0 + e < it.j1) {
+          rows[e] = __ldg(a.kv_indices + it.kv0 + pos0 + e);
+          live |= 1 << e;
+        }
+      }
+    };
+    // Range-check loaded slots: a bad one is flagged and gathered as an
+    // out-of-range row (zeros).
+    auto take_rows = [&](const int (&raw)[4], int live, int (&rows)[4]) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         int slot = oob;
-        if (pos0 + e < it.j1) {
-          const int v = __ldg(a.kv_indices + it.kv0 + pos0 + e);
+        if ((live >> e) & 1) {
+          const int v = raw[e];
           if (v >= 0 && v < a.num_slots) slot = v;
           else flag(a.status, MT_DEV_BAD_SLOT);
         }
@@ -377,34 +414,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pw == 0 && lane == 0) {
         mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort);
         mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTx);
-        for (int k = 0; k < 4; ++k)
-          tma_load_2d(sm + kQLat + k * BM * 128, &tm_qlat, 256 * (int)cta + 64 * k, qrow,
-                      &bars[B_Q_FULL]);
         tma_load_2d(sm + kQRope, &tm_qrope, 512 + 32 * (int)cta, qrow, &bars[B_Q_FULL]);
       }
       ++qi;
-      int next_rows[4] = {oob, oob, oob, oob};
-      if (gathers) load_rows(it, 0, next_rows);
-      for (int blk = 0; blk < it.nblocks; ++blk, ++kb) {
-        const int s = kb % kStages;
-        uint8_t* st = sm + kKV + s * kKVStage;
-        if (lane == 0) {
-          mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort);
-          if (pw == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
-        }
-        __syncwarp();
-        if (gathers) {
-          const int rows[4] = {next_rows[0], next_rows[1], next_rows[2], next_rows[3]};
+      // Slot numbers run kSlotAhead blocks ahead of the gathers. The block
+      // loop is unrolled by kSlotAhead so that ring entry u always holds the
+      // slots of blocks u, u + kSlotAhead, ...: an entry is reloaded right
+      // after its gathers are issued and is not touched again until its
+      // block comes up (moving an entry whose load is still in flight would
+      // wait for it).
+      int ring[kSlotAhead][4], live[kSlotAhead];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tma_gather4(st + k * kKVLat + grp * 512, &tm_kvlat, 256 * (int)cta + 64 * k, rows[0],
-                        rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
-          tma_gather4(st + 4 * kKVLat + grp * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
-                      rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
-          // the next block's slots load while this block's rows are in flight
-          if (blk + 1 < it.nblocks) load_rows(it, blk + 1, next_rows);
+      for (int d = 0; d < kSlotAhead; ++d) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ring[d][e] = oob;
+        live[d] = 0;
+        if (gathers && d < it.nblocks) load_rows(it, d, ring[d], live[d]);
+      }
+      for (int blk0 = 0; blk0 < it.nblocks; blk0 += kSlotAhead) {
+#pragma unroll
+        for (int u = 0; u < kSlotAhead; ++u) {
+          const int blk = blk0 + u;
+          if (blk < it.nblocks) {
+            const int s = kb % kStages;
+            uint8_t* st = sm + kKV + s * kKVStage;
+            if (lane == 0) {
+              mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort);
+              if (pw == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
+            }
+            __syncwarp();
+            if (gathers) {
+              int rows[4];
+              take_rows(ring[u], live[u], rows);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                tma_gather4(st + k * kKVLat + grp * 512, &tm_kvlat, 256 * (int)cta + 64 * k,
+                            rows[0], rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
+              tma_gather4(st + 4 * kKVLat + grp * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
+                          rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
+              live[u] = 0;
+              if (blk + kSlotAhead < it.nblocks) load_rows(it, blk + kSlotAhead, ring[u], live[u]);
+            }
+            __syncwarp();
+            ++kb;
+          }
         }
-        __syncwarp();
       }
     }
     if (pw == 0 && lane == 0) {  // every copy this CTA issued has landed before it may exit
@@ -418,54 +472,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kb = 0, sc = 0, pc = 0, qi = 0, ii = 0;
       const uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, 256, 0, 1);
-      const uint32_t qlat = smem_u32(sm + kQLat), qrope = smem_u32(sm + kQRope);
+      const uint32_t qrope = smem_u32(sm + kQRope);
       const uint32_t kvbase = smem_u32(sm + kKV);
       for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
         const Item it = decode_item(plan, ord, obase, a.batch, id);
         mbar_wait<false>(&bars[B_Q_FULL], qi & 1, abort);
+        mbar_wait<false>(&bars[B_QT_FULL], qi & 1, abort);
         ++qi;
         tc_fence_after();
         const uint32_t kb0 = kb;
-        for (int blk = -1; blk < it.nblocks; ++blk) {
-          // scores of block blk+1 go first so they overlap the softmax of block blk
-          if (blk + 1 < it.nblocks) {
-            const uint32_t kbi = kb0 + blk + 1;
+        // Two independent streams, polled without blocking: S_j = Q K_j^T
+        // as soon as key block j has landed and a score buffer is free
+        // (both are read by the senders early), and O += P_j V_j as soon as
+        // the softmax has written P_j. Waiting for P_j before issuing the
+        // next scores would tie every block to the softmax two blocks back.
+        int nq = 0, np = 0;
+        bool ofree = false;
+        long long idle_since = 0;
+        while (np < it.nblocks) {
+          bool did = false;
+          if (nq < it.nblocks) {
+            const uint32_t kbi = kb0 + nq;
             const uint32_t s = kbi % kStages, sb = sc & 1;
-            mbar_wait<false>(&bars[B_KV_FULL0 + s], (kbi / kStages) & 1, abort);
-            mbar_wait<false>(&bars[B_S_EMPTY0 + sb], ((sc >> 1) & 1) ^ 1, abort);
-            tc_fence_after();
-            const uint32_t stg = kvbase + s * kKVStage;
-            const uint32_t d = tmem + kTmemS + 64 * sb;
+            if (mbar_test_wait(&bars[B_KV_FULL0 + s], (kbi / kStages) & 1) &&
+                mbar_test_wait(&bars[B_S_EMPTY0 + sb], ((sc >> 1) & 1) ^ 1)) {
+              tc_fence_after();
+              const uint32_t stg = kvbase + s * kKVStage;
+              const uint32_t d = tmem + kTmemS + 64 * sb;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+              for (int k = 0; k < 16; ++k)  // latent dims 16k.. from TMEM, keys' 64-dim chunk k/4
+                mma_bf16_ts(d, tmem + kTmemQ + 8 * k,
+                            smem_desc(stg + (k >> 2) * kKVLat + 32 * (k & 3), 16, 1024, kSwizzle128B),
+                            idesc_qk, k != 0);
 #pragma unroll
-              for (int t = 0; t < 4; ++t)
-                mma_bf16_ss(d, smem_desc(qlat + k * BM * 128 + 32 * t, 16, 1024, kSwizzle128B),
-                            smem_desc(stg + k * kKVLat + 32 * t, 16, 1024, kSwizzle128B), idesc_qk,
-                            (k | t) != 0);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              mma_bf16_ss(d, smem_desc(qrope + 32 * t, 16, 512, kSwizzle64B),
-                          smem_desc(stg + 4 * kKVLat + 32 * t, 16, 512, kSwizzle64B), idesc_qk, 1);
-            mma_commit(&bars[B_S_FULL0 + sb]);
-            ++sc;
-            if (blk + 2 == it.nblocks) mma_commit(&bars[B_Q_EMPTY]);  // last use of Q
+              for (int t = 0; t < 2; ++t)
+                mma_bf16_ss(d, smem_desc(qrope + 32 * t, 16, 512, kSwizzle64B),
+                            smem_desc(stg + 4 * kKVLat + 32 * t, 16, 512, kSwizzle64B), idesc_qk, 1);
+              mma_commit(&bars[B_S_FULL0 + sb]);
+              ++sc;
+              if (++nq == it.nblocks) mma_commit(&bars[B_Q_EMPTY]);  // last use of Q
+              did = true;
+            }
           }
-          if (blk < 0) continue;
-          if (blk == 0) mbar_wait<false>(&bars[B_O_FREE], (ii & 1) ^ 1, abort);
-          mbar_wait<false>(&bars[B_P_FULL], pc & 1, abort);
-          tc_fence_after();
-          const uint32_t s = (kb0 + blk) % kStages;
-          const uint32_t stg = kvbase + s * kKVStage;
+          if (np < nq) {
+            if (!ofree) ofree = mbar_test_wait(&bars[B_O_FREE], (ii & 1) ^ 1);
+            if (ofree && mbar_test_wait(&bars[B_P_FULL], pc & 1)) {
+              tc_fence_after();
+              const uint32_t s = (kb0 + np) % kStages;
+              const uint32_t stg = kvbase + s * kKVStage;
 #pragma unroll
-          for (int t = 0; t < BN / 16; ++t)
-            mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * t,
-                        smem_desc(stg + t * 2048, kKVLat, 1024, kSwizzle128B), idesc_pv,
-                        (blk | t) != 0);
-          mma_commit(&bars[B_KV_EMPTY0 + s]);
-          mma_commit(&bars[B_O_DONE]);
-          ++pc;
+              for (int t = 0; t < BN / 16; ++t)
+                mma_bf16_ts(tmem + kTmemO, tmem + tmem_p_col(t),
+                            smem_desc(stg + t * 2048, kKVLat, 1024, kSwizzle128B), idesc_pv,
+                            (np | t) != 0);
+              mma_commit(&bars[B_KV_EMPTY0 + s]);
+              mma_commit(&bars[B_O_DONE]);
+              ++pc;
+              ++np;
+              did = true;
+            }
+          }
+          if (did) {
+            idle_since = 0;
+          } else {  // nothing ready: bounded like every other wait
+            if (*abort) break;
+            const long long now = clock64();
+            if (idle_since == 0) idle_since = now;
+            else if (now - idle_since > kIdleLimitCycles) {
+              *abort = 1;
+              break;
+            }
+          }
         }
         kb += it.nblocks;
         ++ii;
@@ -488,11 +566,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale2 = a.sm_scale * kLog2e;
     const uint32_t xp_peer0 = mapa(smem_u32(sm + kX + kXBytes + r * kXRow), peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
-    uint32_t g = 0;
+    uint32_t g = 0, qi = 0;
+    const int64_t q_rows = (int64_t)a.total_q * H;
     cluster_wait();  // the peer's barriers are initialised
     for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
       const Item it = decode_item(plan, ord, obase, a.batch, id);
+      {
+        // Row r of the query tile, this CTA's 256 latent dims, into TMEM as
+        // bf16 pairs (QK's A operand) once the previous item's last QK is done.
+        // Rows past the last query row read as zeros.
+        const int64_t qrow = (int64_t)it.q0 * H + it.row0 + r;
+        const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * kDqk + 256 * cta);
+        const bool in = qrow < q_rows;
+        mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort);
+        ++qi;
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 v[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = in ? __ldg(src + 16 * half + k) : make_uint4(0, 0, 0, 0);
+          uint32_t w0[32], w1[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            w0[4 * k] = v[k].x; w0[4 * k + 1] = v[k].y; w0[4 * k + 2] = v[k].z; w0[4 * k + 3] = v[k].w;
+            w1[4 * k] = v[8 + k].x; w1[4 * k + 1] = v[8 + k].y;
+            w1[4 * k + 2] = v[8 + k].z; w1[4 * k + 3] = v[8 + k].w;
+          }
+          tmem_st32(tmem + lane_base + kTmemQ + 64 * half, w0);
+          tmem_st32(tmem + lane_base + kTmemQ + 64 * half + 32, w1);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[B_QT_FULL]);
+      }
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1;
         mbar_wait<false>(&bars[B_S_FULL0 + b], (g >> 1) & 1, abort);
@@ -538,19 +646,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO;
-    const uint32_t t_p = tmem + lane_base + kTmemP;
     const uint32_t xfree_peer0 = mapa(smem_u32(&bars[B_X_FREE0]), peer);
     const int64_t R = (int64_t)a.total_q * H;
     uint32_t pw = 0, gblk = 0;
     cluster_wait();  // the peer's barriers are initialised
 
-    // Give buffer pair g & 1 back once all 128 rows have read it: to our own
-    // senders (XO) and to the peer's (our XP is theirs to fill). Every row's
-    // reads are complete here (their values were consumed before the
-    // barrier), so the remote signal needs no release fence.
+    // Give this warp's rows of buffer pair g & 1 back: to our own senders
+    // (XO) and to the peer's (our XP is theirs to fill); the pair is free
+    // once all four warps of both CTAs have signalled. The rows' reads are
+    // complete here (their values were consumed before the signal), so the
+    // remote signal needs no release fence.
     auto release_x = [&](uint32_t g) {
-      named_bar_sync(2, 128);
-      if (r == 0) {
+      __syncwarp();
+      if (lane == 0) {
         mbar_arrive(&bars[B_X_FREE0 + (g & 1)]);
         mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
       }
@@ -643,14 +751,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // masked online softmax (log2 domain)
         const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
-        float mb = -INFINITY;
+        float mx[8];  // eight independent running maxima, then a tree
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
           const float v = bit ? s[c] : -INFINITY;
           s[c] = v;
-          mb = fmaxf(mb, v);
+          mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
         }
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         float corr = 1.f;
         bool resc = false;
         if (mb > m + kRescale) {
@@ -658,10 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mb;
           resc = true;
         }
-        float rs = 0.f;
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = BN / 2; c < 32; ++c) pk[c] = 0u;  // columns past the block are not read
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[BN / 2];
         if (m == -INFINITY) {
 #pragma unroll
           for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
@@ -672,11 +780,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
             // the denominator sums the same bf16 weights the P.V product uses,
             // so O / l stays a true weighted average of the value rows
-            rs += __low2float(v) + __high2float(v);
+            rs4[c & 3] += __low2float(v) + __high2float(v);
             pk[c] = *reinterpret_cast<const uint32_t*>(&v);
           }
         }
-        l = l * corr + rs;
+        l = l * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
 
         // the previous P.V is done: P and O may be touched
         if (blk > 0) {
@@ -696,7 +804,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(t_o + 32 * k, o);
           }
         }
-        tmem_st32(t_p, pk);  // row r of P: 64 bf16 weights as 32 packed columns
+        {  // row r of P: 48 bf16 weights as 24 packed columns, in two pieces
+          uint32_t p01[16], p2[8];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) p01[c] = pk[c];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) p2[c] = pk[16 + c];
+          tmem_st16(tmem + lane_base + tmem_p_col(0), p01);
+          tmem_st8(tmem + lane_base + tmem_p_col(2), p2);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_P_FULL]);
@@ -786,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else a.ws_lse[(int64_t)it.split * R + grow] = lv;
       }
       tc_fence_before();
-      mbar_arrive(&bars[B_O_FREE]);
+      mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
       release_x(glast);  // staging done: the peer may refill this buffer
     }
   }
@@ -875,10 +991,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
     return cudaErrorNotSupported;
   const int nclusters = device_clusters(num_sms > 0 ? num_sms : 148);
   if (nclusters <= 0) return cudaErrorNotSupported;
-  CUtensorMap tq_lat, tq_rope, tkv_lat, tkv_rope;
+  CUtensorMap tq_rope, tkv_lat, tkv_rope;
   const uint64_t qrows = (uint64_t)a.total_q * a.heads;
-  if (!make_map(&tq_lat, a.q, qrows, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tq_rope, a.q, qrows, 32, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_map(&tq_rope, a.q, qrows, 32, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&tkv_lat, a.kv, (uint64_t)a.num_slots, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&tkv_rope, a.kv, (uint64_t)a.num_slots, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorNotSupported;
@@ -898,7 +1013,7 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, p, tq_lat, tq_rope, tkv_lat, tkv_rope);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, p, tq_rope, tkv_lat, tkv_rope);
   if (e != cudaSuccess) return e;
   if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
   return cudaSuccess;

@@ -189,7 +189,7 @@ __device__ __forceinline__ long long warp_sum(long long v) {
 }
 
 // Warp 0: per-request geometry, split counts and the item numbering. Every
-// CTA computes the same plan from the device indptrs; CTA 0 also publishes
+// CTA computes the same plan from the device indptrs; one CTA also publishes
 // the split counts for the merge kernel.
 //
 // Split length: a quarter of one cluster's fair share of (tile x key) work,
@@ -351,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_kvlat);
     prefetch_tmap(&tm_kvrope);
   }
-  if (warp == 0) build_plan(a, p.nclusters, plan, ord, obase, total_items_s, lane, blockIdx.x == 0);
+  // the last CTA publishes the split counts: with fewer items than clusters it
+  // has none of its own, so the extra stores delay no item
+  if (warp == 0)
+    build_plan(a, p.nclusters, plan, ord, obase, total_items_s, lane, blockIdx.x == gridDim.x - 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

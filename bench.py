@@ -141,6 +141,25 @@ def _traffic(kernel):
     return None
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of x over all ranks of the default process group (x itself
+    when not distributed). The step time of a multi-GPU run is the slowest
+    rank's: every rank replays the same workload on its own GPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, steps, kv_bytes, total_ms):
+    """Aggregate KV GB/s of a weak-scaling run: every rank reads kv_bytes per
+    step, the job takes the slowest rank's time."""
+    return world * steps * kv_bytes / (total_ms * 1e-3) / 1e9
+
+
 def cpu_baseline(cid, budget_s, one_request=False, steps=None):
     """Time the fp64 oracle on this host's cores; returns (GB/s, seconds, sample text)."""
     import numpy as np
@@ -289,15 +308,11 @@ def run_ours(args):
 
     step_ms = [e[0].elapsed_time(e[4]) for e in events]
     call_ms = [[e[i].elapsed_time(e[i + 1]) for e in events] for i in range(4)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     assert int(st.status.item()) == 0
 
     kv_bytes = w.kv_bytes()
-    value = world * args.steps * kv_bytes / (total_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, args.steps, kv_bytes, total_ms)
     byts, flops = alg_cost(w)
     verify_ms = statistics.mean(call_ms[3])
     hbm, tf_burst, tf_sus, which = _peaks()
@@ -331,12 +346,8 @@ def run_ours(args):
                 if e:
                     e[1].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * args.steps * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev), dev)
+        e2e = {"value": whole_job_gbs(world, args.steps, kv_bytes, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps}
 

@@ -23,6 +23,7 @@ from .tree_verify import (  # noqa: F401
     kv_indices_build,
     ancestors_or_self,
     tree_mask_pack,
+    tree_mask_pack_bits,
     verify_attention,
     verify_attention_split,
     lse_merge,

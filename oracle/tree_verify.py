@@ -142,6 +142,42 @@ def tree_mask_pack(parents, qo_indptr, kv_indptr):
     return np.array(mask_indptr, dtype=np.int64), packed
 
 
+def tree_mask_pack_bits(parents, qo_indptr, kv_indptr):
+    """The same visibility as ``tree_mask_pack``, one bit per (row, column).
+
+    "Pivot to Live Cutover" page, section "The Technical Investigation:
+    Probing the Integration Surface", calls the custom mask a packed bitmask.
+    This encoding keeps that literal reading next to the byte-per-element
+    one: row i of request b holds its L_b visibility bits, column j in bit
+    j % 32 of word j // 32 (least significant bit first), in
+    W_b = ceil(L_b / 32) uint32 words; bits past L_b are zero. Rows follow
+    each other, requests too: row i of request b starts at word
+    mask_word_indptr[b] + i * W_b.
+    Returns (mask_word_indptr int64 [B+1], mask_words uint32 [mask_word_indptr[B]]).
+    """
+    par = _as_np(parents).astype(np.int64)
+    qptr = _as_np(qo_indptr).astype(np.int64)
+    kptr = _as_np(kv_indptr).astype(np.int64)
+    batch = len(qptr) - 1
+    indptr = [0]
+    chunks = []
+    for b in range(batch):
+        n = int(qptr[b + 1] - qptr[b])
+        L = int(kptr[b + 1] - kptr[b])
+        P = L - n
+        W = (L + 31) // 32
+        vis = ancestors_or_self(par[qptr[b]:qptr[b + 1]])
+        words = np.zeros((n, W), dtype=np.uint64)
+        for i in range(n):
+            cols = list(range(P)) + [P + k for k in vis[i]]
+            for j in cols:
+                words[i, j // 32] |= np.uint64(1) << np.uint64(j % 32)
+        chunks.append(words.astype(np.uint32).reshape(-1))
+        indptr.append(indptr[-1] + n * W)
+    packed = np.concatenate(chunks) if chunks else np.zeros(0, dtype=np.uint32)
+    return np.array(indptr, dtype=np.int64), packed
+
+
 def _request_rows(qptr, heads, rows):
     """Group requested (token, head) rows by request; None = all rows."""
     batch = len(qptr) - 1

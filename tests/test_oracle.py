@@ -108,6 +108,42 @@ def test_mask_chain_is_causal_and_star_is_diagonal():
     assert (star == diag).all()
 
 
+def test_small_tree_mask_bits_by_hand():
+    """The bit encoding of the hand-worked masks (words also worked by hand)."""
+    g = json.load(open(os.path.join(GOLDEN, "small_tree_mask.json")))
+    parents, qo, kv = [], [0], [0]
+    for r in g["requests"]:
+        parents += r["parents"]
+        qo.append(qo[-1] + len(r["parents"]))
+        kv.append(kv[-1] + r["prefix"] + len(r["parents"]))
+    indptr, words = oracle.tree_mask_pack_bits(np.array(parents), np.array(qo), np.array(kv))
+    assert indptr.tolist() == g["mask_word_indptr"]
+    assert words.dtype == np.uint32
+    assert words.tolist() == g["mask_words"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_mask_bits_unpack_to_mask_bytes(seed):
+    """Rows of several words (prefixes 0..130, trees up to 40 nodes): unpacking
+    each row's words with numpy's bit order gives the byte mask, and the bits
+    past the row's last column are zero."""
+    rng = np.random.default_rng(seed)
+    batch = 5
+    n = rng.integers(1, 41, batch)
+    P = rng.integers(0, 131, batch)
+    parents = np.concatenate([[int(rng.integers(-1, i)) for i in range(k)] for k in n])
+    qo = np.concatenate([[0], np.cumsum(n)])
+    kv = np.concatenate([[0], np.cumsum(n + P)])
+    bi, words = oracle.tree_mask_pack_bits(parents, qo, kv)
+    mi, mask = oracle.tree_mask_pack(parents, qo, kv)
+    for b in range(batch):
+        L, W = int(n[b] + P[b]), int((n[b] + P[b] + 31) // 32)
+        rows = words[bi[b]:bi[b + 1]].reshape(int(n[b]), W)
+        bits = np.unpackbits(rows.astype("<u4").view(np.uint8), bitorder="little").reshape(int(n[b]), 32 * W)
+        assert (bits[:, :L] == mask[mi[b]:mi[b + 1]].reshape(int(n[b]), L)).all()
+        assert not bits[:, L:].any()
+
+
 def test_mask_rejects_non_topological_parent():
     with pytest.raises(ValueError):
         oracle.ancestors_or_self([-1, 2, 0])

@@ -3,7 +3,8 @@
 
 A step is one pass of the whole verify path over one batch: draft-KV scatter,
 KV index marshaling, tree-mask packing and tree-verify attention (with its
-split merge). Default workload: 8 requests, prefixes U{1024..4096},
+split merge). The tree mask is packed in its bit form by default (one bit
+per (row, column); --mask bytes uses one byte per element). Default workload: 8 requests, prefixes U{1024..4096},
 16-node draft trees (branching <= 3), 8 heads, 65536-slot pool.
 
 Timing: each of the four calls is captured once as a CUDA graph; a timed
@@ -51,17 +52,18 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def alg_cost(w):
+def alg_cost(w, mask_bits=False):
     """Algorithmic bytes and flops of one verify call: every key row once,
-    its index, the mask bytes, q in, out and lse out; flops over visible
-    (row, key) pairs only."""
+    its index, the mask (a byte, or a bit in whole 32-bit words, per (row,
+    key)), q in, out and lse out; flops over visible (row, key) pairs only."""
     H = w.heads
     qo = w.qo_indptr.tolist()
     byts, flops = 0, 0
     for b in range(w.batch):
         n, P = w.tree_sizes[b], w.prefix_lens[b]
         L = P + n
-        byts += L * 1152 + L * 4 + n * L + n * H * (1152 + 1024 + 4)
+        mask_bytes = n * 4 * ((L + 31) // 32) if mask_bits else n * L
+        byts += L * 1152 + L * 4 + mask_bytes + n * H * (1152 + 1024 + 4)
         par = w.parents[qo[b]:qo[b + 1]].tolist()
         depth = []
         for i, p in enumerate(par):
@@ -247,7 +249,7 @@ def run_ours(args):
     __graft_entry__.build()
 
     w = W.config(args.config)
-    st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path)
+    st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path, mask_bits=args.mask == "bits")
     stream = torch.cuda.Stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
@@ -265,8 +267,7 @@ def run_ours(args):
     calls = [lambda: abi.mla_tree_draft_kv_scatter(st.draft_kv, st.out_cache_loc, st.pool, st.status),
              lambda: abi.mla_tree_kv_indices_build(st.prefix_indices, st.prefix_indptr, st.out_cache_loc,
                                                    st.qo_indptr, st.kv_indices, st.kv_indptr, st.status),
-             lambda: abi.tree_mask_pack(st.parents, st.qo_indptr, st.kv_indptr, st.mask_indptr, st.mask,
-                                        st.status),
+             lambda: st.pack_mask(),
              lambda: st.verify()]
     graphs = []
     for c in calls:
@@ -313,7 +314,7 @@ def run_ours(args):
 
     kv_bytes = w.kv_bytes()
     value = whole_job_gbs(world, args.steps, kv_bytes, total_ms)
-    byts, flops = alg_cost(w)
+    byts, flops = alg_cost(w, args.mask == "bits")
     verify_ms = statistics.mean(call_ms[3])
     hbm, tf_burst, tf_sus, which = _peaks()
     achieved_gbs = byts / (verify_ms * 1e-3) / 1e9
@@ -366,7 +367,7 @@ def run_ours(args):
             "config": {"workload": W.CONFIG_NAMES[args.config], "batch": w.batch, "heads": w.heads,
                        "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
                        "path": ["auto", "simt", "tensor-core"][args.path],
-                       "max_splits": args.max_splits,
+                       "max_splits": args.max_splits, "mask": args.mask,
                        "l2": "flushed between steps: 256 MiB written then read back, outside the events",
                        "timing": "per-call CUDA graphs, CUDA events on the launching stream"},
             "step_ms": {"scatter": statistics.mean(call_ms[0]), "kv_indices": statistics.mean(call_ms[1]),
@@ -401,6 +402,8 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--mask", default="bits", choices=["bytes", "bits"],
+                    help="tree-mask form: one byte or one bit per (row, column)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -140,6 +140,26 @@ int tree_mask_pack(const int32_t* parents, const int32_t* qo_indptr, const int32
                    int32_t* dev_status, mt_stream_t stream);
 
 /*
+ * The same tree mask, one bit per (row, column) ("Pivot to Live Cutover",
+ * "The Technical Investigation": the custom mask is called a packed
+ * bitmask). Row i of request b holds its L_b visibility bits in
+ * W_b = ceil(L_b / 32) uint32 words, column j in bit j % 32 of word j / 32
+ * (least significant bit first); bits past L_b are 0. Writes
+ * mask_word_indptr: int64 [batch+1], mask_word_indptr[b+1] =
+ * mask_word_indptr[b] + n_b * W_b, and mask_words: uint32
+ * [mask_word_indptr[batch]], row i of request b at mask_word_indptr[b] +
+ * i * W_b. Visibility, arguments and error behaviour are those of
+ * tree_mask_pack, with mask_capacity_words counted in words. The bit form
+ * is an eighth of the bytes and lets the verify kernels read a block's
+ * visibility with a few word loads per row.
+ */
+int tree_mask_pack_bits(const int32_t* parents, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                        int batch, int total_q,
+                        int64_t* mask_word_indptr, uint32_t* mask_words,
+                        int64_t mask_capacity_words,
+                        int32_t* dev_status, mt_stream_t stream);
+
+/*
  * Bytes of scratch workspace mla_tree_verify needs for these capacities
  * (max_splits 0 = the automatic choice mla_tree_verify makes for 0).
  * Holds per-split partial outputs (fp32 [splits][total_q*heads][512]), their
@@ -188,6 +208,24 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
                     mt_bf16* out, float* lse,
                     void* workspace, size_t workspace_bytes, int max_splits, int path,
                     int32_t* dev_status, mt_stream_t stream);
+
+/*
+ * mla_tree_verify with the tree mask in the bit form of tree_mask_pack_bits:
+ *     vis_j = (mask_words[mask_word_indptr[b] + i * W_b + j / 32] >> (j % 32)) & 1
+ * with W_b = ceil(L_b / 32); mask_len_words counts the words of mask_words.
+ * Everything else (arguments, outputs, workspace, paths, error behaviour)
+ * is that of mla_tree_verify, and the results are the same as for the
+ * equivalent byte mask.
+ */
+int mla_tree_verify_bits(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                         const int32_t* kv_indices, int64_t kv_indices_len,
+                         const int32_t* kv_indptr, const int32_t* qo_indptr,
+                         const uint32_t* mask_words, int64_t mask_len_words,
+                         const int64_t* mask_word_indptr,
+                         int batch, int total_q, int heads, float sm_scale,
+                         mt_bf16* out, float* lse,
+                         void* workspace, size_t workspace_bytes, int max_splits, int path,
+                         int32_t* dev_status, mt_stream_t stream);
 
 /*
  * mla_tree_verify without a caller-provided workspace. The paper has no

@@ -17,8 +17,9 @@ DEV_BAD_SLOT, DEV_BAD_PARENT, DEV_BAD_INDPTR, DEV_TREE_TOO_BIG, DEV_TIMEOUT = 1,
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 
 EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_scatter",
-           "mla_tree_kv_indices_build", "tree_mask_pack", "mla_tree_verify_workspace_bytes",
-           "mla_tree_verify_launch_count", "mla_tree_verify", "mla_tree_verify_noalloc"]
+           "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits",
+           "mla_tree_verify_workspace_bytes", "mla_tree_verify_launch_count", "mla_tree_verify",
+           "mla_tree_verify_bits", "mla_tree_verify_noalloc"]
 MT_ESCRATCH = -5
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -48,6 +49,8 @@ def load():
     lib.mla_tree_kv_indices_build.argtypes = [P, I64, P, P, P, I32, I32, P, I64, P, P, P]
     lib.tree_mask_pack.restype = I32
     lib.tree_mask_pack.argtypes = [P, P, P, I32, I32, P, P, I64, P, P]
+    lib.tree_mask_pack_bits.restype = I32
+    lib.tree_mask_pack_bits.argtypes = [P, P, P, I32, I32, P, P, I64, P, P]
     lib.mla_tree_verify_workspace_bytes.restype = SZ
     lib.mla_tree_verify_workspace_bytes.argtypes = [I32, I32, I32, I32]
     lib.mla_tree_verify_launch_count.restype = I32
@@ -55,6 +58,9 @@ def load():
     lib.mla_tree_verify.restype = I32
     lib.mla_tree_verify.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                     P, P, P, SZ, I32, I32, P, P]
+    lib.mla_tree_verify_bits.restype = I32
+    lib.mla_tree_verify_bits.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
+                                         P, P, P, SZ, I32, I32, P, P]
     lib.mla_tree_verify_noalloc.restype = I32
     lib.mla_tree_verify_noalloc.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                             P, P, I32, I32, P, P]
@@ -125,6 +131,19 @@ def tree_mask_pack(parents, qo_indptr, kv_indptr, mask_indptr, packed_mask, stat
     _check(rc, "tree_mask_pack")
 
 
+def tree_mask_pack_bits(parents, qo_indptr, kv_indptr, mask_word_indptr, mask_words, status=None,
+                        stream=None):
+    """The same tree mask, one bit per (row, column): rows of ceil(L/32) uint32 words."""
+    batch = qo_indptr.numel() - 1
+    rc = load().tree_mask_pack_bits(
+        _ptr(parents, torch.int32, "parents"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), batch, parents.numel(),
+        _ptr(mask_word_indptr, torch.int64, "mask_word_indptr"),
+        _ptr(mask_words, torch.int32, "mask_words"), mask_words.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "tree_mask_pack_bits")
+
+
 def mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits=0):
     return int(load().mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits))
 
@@ -151,6 +170,27 @@ def mla_tree_verify(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, ma
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, path,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "mla_tree_verify")
+
+
+def mla_tree_verify_bits(q, kv_buf, kv_indices, kv_indptr, qo_indptr, mask_words, mask_word_indptr,
+                         sm_scale, out, lse, workspace, max_splits=0, path=PATH_AUTO, status=None,
+                         stream=None):
+    """mla_tree_verify with the mask in the bit form of tree_mask_pack_bits
+    (mask_words: int32 tensor holding the uint32 words)."""
+    if q.dim() != 3 or q.shape[2] != 576:
+        raise MlaTreeError("q must be [total_q, heads, 576]")
+    total_q, heads = q.shape[0], q.shape[1]
+    batch = qo_indptr.numel() - 1
+    rc = load().mla_tree_verify_bits(
+        _ptr(q, torch.bfloat16, "q"), _ptr(kv_buf, torch.bfloat16, "kv_buf"), kv_buf.shape[0],
+        _ptr(kv_indices, torch.int32, "kv_indices"), kv_indices.numel(),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(mask_words, torch.int32, "mask_words"), mask_words.numel(),
+        _ptr(mask_word_indptr, torch.int64, "mask_word_indptr"), batch, total_q, heads,
+        float(sm_scale), _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, path,
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "mla_tree_verify_bits")
 
 
 def mla_tree_verify_noalloc(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, mask_indptr,

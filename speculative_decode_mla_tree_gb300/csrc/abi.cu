@@ -119,6 +119,20 @@ int tree_mask_pack(const int32_t* parents, const int32_t* qo_indptr, const int32
                                            sm_count(), (cudaStream_t)stream));
 }
 
+int tree_mask_pack_bits(const int32_t* parents, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                        int batch, int total_q, int64_t* mask_word_indptr, uint32_t* mask_words,
+                        int64_t mask_capacity_words, int32_t* dev_status, mt_stream_t stream) {
+  if (batch < 0 || total_q < 0 || mask_capacity_words < 0) return MT_EINVAL;
+  if (batch == 0) return MT_OK;
+  if (!qo_indptr || !kv_indptr || !mask_word_indptr) return MT_EINVAL;
+  if (total_q > 0 && !parents) return MT_EINVAL;
+  if (mask_capacity_words > 0 && !mask_words) return MT_EINVAL;
+  if (batch > 65535) return MT_EUNSUPPORTED;
+  return cuda_status(launch_tree_mask_pack_bits(parents, qo_indptr, kv_indptr, batch, total_q,
+                                                mask_word_indptr, mask_words, mask_capacity_words,
+                                                dev_status, sm_count(), (cudaStream_t)stream));
+}
+
 size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int max_splits) {
   if (batch < 0 || total_q < 0 || heads < 0 || max_splits < 0 || max_splits > MT_MAX_SPLITS) return 0;
   if (max_splits == 0) max_splits = auto_max_splits(batch, total_q, heads, sm_count());
@@ -140,12 +154,18 @@ int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_spli
   return max_splits > 1 ? 2 : 1;
 }
 
-int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
-                    const int32_t* kv_indices, int64_t kv_indices_len, const int32_t* kv_indptr,
-                    const int32_t* qo_indptr, const uint8_t* packed_mask, int64_t mask_len,
-                    const int64_t* mask_indptr, int batch, int total_q, int heads, float sm_scale,
-                    mt_bf16* out, float* lse, void* workspace, size_t workspace_bytes,
-                    int max_splits, int path, int32_t* dev_status, mt_stream_t stream) {
+}  // extern "C"
+
+// One verify call with either mask form: bits = 0 uses packed_mask (bytes),
+// bits = 1 uses mask_words; mask_len counts the elements of that mask.
+static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                         const int32_t* kv_indices, int64_t kv_indices_len,
+                         const int32_t* kv_indptr, const int32_t* qo_indptr, int bits,
+                         const uint8_t* packed_mask, const uint32_t* mask_words, int64_t mask_len,
+                         const int64_t* mask_indptr, int batch, int total_q, int heads,
+                         float sm_scale, mt_bf16* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int max_splits, int path, int32_t* dev_status,
+                         mt_stream_t stream) {
   if (batch < 0 || total_q < 0 || heads <= 0 || num_slots < 0 || kv_indices_len < 0 ||
       mask_len < 0 || max_splits < 0 || max_splits > MT_MAX_SPLITS || path < 0 || path > 2)
     return MT_EINVAL;
@@ -153,7 +173,7 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
   if (batch == 0 || total_q == 0) return MT_OK;
   if (!q || !kv_buf || !kv_indptr || !qo_indptr || !mask_indptr || !out || !lse) return MT_EINVAL;
   if (kv_indices_len > 0 && !kv_indices) return MT_EINVAL;
-  if (mask_len > 0 && !packed_mask) return MT_EINVAL;
+  if (mask_len > 0 && (bits ? !mask_words : !packed_mask)) return MT_EINVAL;
   if ((uintptr_t)q % 16 || (uintptr_t)kv_buf % 16 || (uintptr_t)out % 16 || (uintptr_t)lse % 4)
     return MT_EINVAL;
   if ((long long)total_q * heads > (1LL << 31) / MT_D_V) return MT_EUNSUPPORTED;
@@ -170,7 +190,9 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
   a.kv_len = kv_indices_len;
   a.kv_indptr = kv_indptr;
   a.qo_indptr = qo_indptr;
-  a.mask = packed_mask;
+  a.mask = bits ? nullptr : packed_mask;
+  a.mask_bits = bits ? mask_words : nullptr;
+  a.bits_mask = bits ? 1 : 0;
   a.mask_len = mask_len;
   a.mask_indptr = mask_indptr;
   a.batch = batch;
@@ -207,6 +229,34 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
   if (e != cudaSuccess) return MT_ECUDA;
   if (max_splits > 1) e = launch_lse_merge(a, s);
   return cuda_status(e);
+}
+
+extern "C" {
+
+int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                    const int32_t* kv_indices, int64_t kv_indices_len, const int32_t* kv_indptr,
+                    const int32_t* qo_indptr, const uint8_t* packed_mask, int64_t mask_len,
+                    const int64_t* mask_indptr, int batch, int total_q, int heads, float sm_scale,
+                    mt_bf16* out, float* lse, void* workspace, size_t workspace_bytes,
+                    int max_splits, int path, int32_t* dev_status, mt_stream_t stream) {
+  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 0,
+                       packed_mask, nullptr, mask_len, mask_indptr, batch, total_q, heads,
+                       sm_scale, out, lse, workspace, workspace_bytes, max_splits, path,
+                       dev_status, stream);
+}
+
+int mla_tree_verify_bits(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                         const int32_t* kv_indices, int64_t kv_indices_len,
+                         const int32_t* kv_indptr, const int32_t* qo_indptr,
+                         const uint32_t* mask_words, int64_t mask_len_words,
+                         const int64_t* mask_word_indptr, int batch, int total_q, int heads,
+                         float sm_scale, mt_bf16* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int max_splits, int path, int32_t* dev_status,
+                         mt_stream_t stream) {
+  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 1,
+                       nullptr, mask_words, mask_len_words,
+                       mask_word_indptr, batch, total_q, heads, sm_scale, out, lse, workspace,
+                       workspace_bytes, max_splits, path, dev_status, stream);
 }
 
 }  // extern "C"

@@ -248,4 +248,108 @@ cudaError_t launch_tree_mask_pack(const int32_t* parents, const int32_t* qptr, c
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- bit-form mask
+// The same visibility, one bit per (row, column): row i of request b in
+// W = ceil(L / 32) words, column j in bit j % 32 of word j / 32. Words wholly
+// inside the prefix are all ones; only the few words that reach the draft
+// columns read the row's ancestor set.
+__global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_bits_kernel(
+    const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
+    const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ word_indptr,
+    uint32_t* __restrict__ words, int64_t capacity, int32_t* status) {
+  __shared__ uint32_t bits[MT_MAX_TREE / 32];
+  __shared__ long long s_base;
+  __shared__ int s_bad;
+  const int b = blockIdx.y;
+  if (threadIdx.x == 0) {
+    long long base = 0;
+    int bad = 0;
+    for (int r = 0; r < b; ++r) {
+      const long long n = (long long)qptr[r + 1] - qptr[r];
+      const long long L = (long long)kptr[r + 1] - kptr[r];
+      if (n < 0 || L < n) bad = 1;
+      base += n * ((L + 31) >> 5);
+    }
+    s_base = base;
+    s_bad = bad;
+    if (b == 0 && blockIdx.x == 0) {
+      long long acc = 0;
+      word_indptr[0] = 0;
+      for (int r = 0; r < batch; ++r) {
+        const long long n = (long long)qptr[r + 1] - qptr[r];
+        const long long L = (long long)kptr[r + 1] - kptr[r];
+        acc += (n >= 0 && L >= n) ? n * ((L + 31) >> 5) : 0;
+        word_indptr[r + 1] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t q0 = qptr[b];
+  const int64_t n = (int64_t)qptr[b + 1] - q0;
+  const int64_t L = (int64_t)kptr[b + 1] - kptr[b];
+  const int64_t P = L - n;
+  const int64_t W = (L + 31) >> 5;
+  const int64_t base = s_base;
+  if (s_bad || n < 0 || P < 0 || q0 < 0 || q0 + n > total_q || base + n * W > capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
+    return;
+  }
+  if (n > MT_MAX_TREE) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_TREE_TOO_BIG);
+    return;
+  }
+  const int nwords = (int)((n + 31) >> 5);
+  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+    for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // Ancestor-or-self walk; parents strictly decrease, so at most n steps.
+      int64_t k = i;
+      while (k >= 0) {
+        bits[k >> 5] |= 1u << (k & 31);
+        const int32_t p = parents[q0 + k];
+        if (p < -1 || p >= k) {
+          flag(status, MT_DEV_BAD_PARENT);
+          break;
+        }
+        k = p;
+      }
+    }
+    __syncthreads();
+    uint32_t* row = words + base + i * W;
+    for (int64_t w = threadIdx.x; w < W; w += blockDim.x) {
+      const int64_t c0 = w << 5;
+      uint32_t v;
+      if (c0 + 32 <= P) {
+        v = 0xffffffffu;
+      } else {
+        v = 0u;
+#pragma unroll 4
+        for (int e = 0; e < 32; ++e) {
+          const int64_t col = c0 + e;
+          uint32_t on = 0;
+          if (col < P) on = 1;
+          else if (col < L) on = (bits[(col - P) >> 5] >> ((col - P) & 31)) & 1u;
+          v |= on << e;
+        }
+      }
+      row[w] = v;
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_tree_mask_pack_bits(const int32_t* parents, const int32_t* qptr,
+                                       const int32_t* kptr, int batch, int total_q,
+                                       int64_t* word_indptr, uint32_t* words, int64_t capacity,
+                                       int32_t* status, int num_sms, cudaStream_t stream) {
+  int groups = (2 * num_sms + batch - 1) / batch;
+  if (groups < 1) groups = 1;
+  if (groups > 64) groups = 64;
+  dim3 grid(groups, batch);
+  tree_mask_pack_bits_kernel<<<grid, kMaskThreads, 0, stream>>>(parents, qptr, kptr, batch, total_q,
+                                                                word_indptr, words, capacity, status);
+  return cudaGetLastError();
+}
+
 }  // namespace mt

@@ -38,13 +38,16 @@ struct ReqGeom {
   int L;           // key positions
   int n;           // draft rows
   int64_t q0;      // first token
-  int64_t mask0;   // first mask byte
+  int64_t mask0;   // first mask element (byte, or word of the bit form)
+  int mask_row;    // mask elements per draft row: L (bytes) or ceil(L / 32) (words)
   bool ok;
 };
 
+// mask_bits: the mask is in the bit form (rows of ceil(L / 32) uint32 words).
 __device__ __forceinline__ ReqGeom request_geom(const int32_t* kv_indptr, const int32_t* qo_indptr,
                                                 const int64_t* mask_indptr, int b,
-                                                int64_t kv_len, int64_t mask_len, int total_q) {
+                                                int64_t kv_len, int64_t mask_len, int total_q,
+                                                bool mask_bits = false) {
   ReqGeom g;
   g.kv0 = kv_indptr[b];
   int64_t kv1 = kv_indptr[b + 1];
@@ -53,9 +56,10 @@ __device__ __forceinline__ ReqGeom request_geom(const int32_t* kv_indptr, const 
   g.mask0 = mask_indptr[b];
   g.L = (int)(kv1 - g.kv0);
   g.n = (int)(q1 - g.q0);
+  g.mask_row = mask_bits ? (g.L + 31) >> 5 : g.L;
   g.ok = g.kv0 >= 0 && kv1 >= g.kv0 && kv1 <= kv_len && g.q0 >= 0 && q1 >= g.q0 &&
          q1 <= total_q && g.mask0 >= 0 && g.n <= g.L &&
-         g.mask0 + (int64_t)g.n * g.L <= mask_len;
+         g.mask0 + (int64_t)g.n * g.mask_row <= mask_len;
   return g;
 }
 

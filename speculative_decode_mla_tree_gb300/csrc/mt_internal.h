@@ -15,8 +15,10 @@ struct VerifyArgs {
   int64_t kv_len;
   const int32_t* kv_indptr;
   const int32_t* qo_indptr;
-  const uint8_t* mask;
-  int64_t mask_len;
+  const uint8_t* mask;           // byte mask, or nullptr when mask_bits is set
+  const uint32_t* mask_bits;     // bit-form mask (rows of ceil(L / 32) words)
+  int bits_mask;                 // 1: the mask is mask_bits, 0: it is mask (bytes)
+  int64_t mask_len;              // elements of that mask
   const int64_t* mask_indptr;
   int batch, total_q, heads;
   float sm_scale;
@@ -54,6 +56,11 @@ cudaError_t launch_tree_mask_pack(const int32_t* parents, const int32_t* qptr, c
                                   int batch, int total_q, int64_t* mask_indptr, uint8_t* mask,
                                   int64_t capacity, int32_t* status, int num_sms,
                                   cudaStream_t stream);
+
+cudaError_t launch_tree_mask_pack_bits(const int32_t* parents, const int32_t* qptr,
+                                       const int32_t* kptr, int batch, int total_q,
+                                       int64_t* word_indptr, uint32_t* words, int64_t capacity,
+                                       int32_t* status, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream);

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   const int split = blockIdx.y;
   const int b = find_request(a.qo_indptr, a.batch, t);
   const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
-                                 a.mask_len, a.total_q);
+                                 a.mask_len, a.total_q, a.bits_mask != 0);
   if (!g.ok || t < g.q0 || t >= g.q0 + g.n) {
     if (lane == 0 && split == 0) {
       flag(a.status, MT_DEV_BAD_INDPTR);
@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
     for (int e = 0; e < 16; ++e) acc[r][e] = 0.f;
   }
 
-  const uint8_t* mrow = a.mask + g.mask0 + (t - g.q0) * (int64_t)g.L;
+  // this token's mask row: L bytes, or ceil(L / 32) words of the bit form
+  const int64_t mrow0 = g.mask0 + (t - g.q0) * (int64_t)g.mask_row;
   const int32_t* idx = a.kv_indices + g.kv0;
   for (int j = j0; j < j1; ++j) {
     const int32_t slot = __ldg(idx + j);
@@ -103,7 +104,9 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
       if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
       continue;
     }
-    if (!__ldg(mrow + j)) continue;
+    const bool vis = a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u)
+                                  : __ldg(a.mask + mrow0 + j) != 0;
+    if (!vis) continue;
     float kf[18];
     load_row18(a.kv + (int64_t)slot * kDqk, lane, 1.f, kf);
 #pragma unroll

@@ -201,7 +201,7 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
   long long units = 0;
   for (int b = lane; b < a.batch; b += 32) {
     const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
-                                   a.mask_len, a.total_q);
+                                   a.mask_len, a.total_q, a.bits_mask != 0);
     int* pr = plan + b * kPlanStride;
     int tiles = 0;
     if (g.ok && g.n > 0) tiles = (int)(((long long)g.n * H + BM - 1) / BM);
@@ -296,6 +296,8 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
   }
 }
 
+// kBits: the tree mask is in the bit form (rows of ceil(L / 32) words)
+template <bool kBits>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ TcParams p,
                      const __grid_constant__ CUtensorMap tm_qrope,
@@ -698,10 +700,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (prefetch) load_mask(0);
+      // Bit-form mask: this row's node reads the (up to) three words holding
+      // a block's 48 columns straight from global memory, one block ahead.
+      const int mw = (it.L + 31) >> 5;
+      const uint32_t* mrow = kBits ? a.mask_bits + it.mask0 + (int64_t)node * mw : nullptr;
+      uint32_t mnext[3] = {0u, 0u, 0u};
+      auto load_bits = [&](int blk_) {
+        const int wi = (it.j0 + blk_ * BN) >> 5;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) mnext[k] = wi + k < mw ? __ldg(mrow + wi + k) : 0u;
+      };
+      if (kBits) load_bits(0);
+      else if (prefetch) load_mask(0);
       float m = -INFINITY, l = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++gblk) {
         const int jb = it.j0 + blk * BN;
+        uint64_t vm;
+        if (kBits) {
+          const uint32_t w0 = mnext[0], w1 = mnext[1], w2 = mnext[2];
+          if (blk + 1 < it.nblocks) load_bits(blk + 1);
+          const int o = jb & 31;
+          const uint64_t lo = (uint64_t)w0 | ((uint64_t)w1 << 32);
+          vm = o ? (lo >> o) | ((uint64_t)w2 << (64 - o)) : lo;
+          const int lim = it.j1 - jb;  // columns of this block inside the split
+          if (lim < 64) vm &= (1ull << lim) - 1ull;
+        } else {
         // visibility bits of this block for the tile's draft nodes
         uint8_t* vb = reinterpret_cast<uint8_t*>(vis + (gblk & 1) * kVisNodes);
         if (prefetch) {
@@ -728,7 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         named_bar_sync(1, 128);
-        const uint64_t vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
+        vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
+        }
 
         // full scores (log2 domain): our fp16 partial plus the peer's
         const uint32_t xb = gblk & 1;
@@ -964,7 +988,9 @@ int device_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(g_dev_mu);
   if (g_clusters[dev] > 0) return g_clusters[dev];
-  if (cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -979,7 +1005,7 @@ int device_clusters(int num_sms) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel, &cfg) != cudaSuccess || n <= 0)
+  if (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<false>, &cfg) != cudaSuccess || n <= 0)
     n = num_sms / 2;
   g_clusters[dev] = n;
   return n;
@@ -1016,7 +1042,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, p, tq_rope, tkv_lat, tkv_rope);
+  cudaError_t e = a.bits_mask
+      ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, p, tq_rope, tkv_lat, tkv_rope)
+      : cudaLaunchKernelEx(&cfg, verify_tc_kernel<false>, p, tq_rope, tkv_lat, tkv_rope);
   if (e != cudaSuccess) return e;
   if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
   return cudaSuccess;

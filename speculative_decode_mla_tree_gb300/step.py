@@ -11,7 +11,8 @@ from . import abi
 
 
 class VerifyStep:
-    def __init__(self, w, device="cuda", max_splits=0, path=abi.PATH_AUTO, pool=None):
+    def __init__(self, w, device="cuda", max_splits=0, path=abi.PATH_AUTO, pool=None,
+                 mask_bits=False):
         dev = torch.device(device)
         self.device = dev
         self.w = w
@@ -19,6 +20,7 @@ class VerifyStep:
         self.sm_scale = w.sm_scale
         self.max_splits = max_splits
         self.path = path
+        self.mask_bits = mask_bits
         B, T = w.batch, w.total_q
         L = [p + n for p, n in zip(w.prefix_lens, w.tree_sizes)]
         # resident latent-KV pool (before the draft rows are scattered in)
@@ -36,6 +38,10 @@ class VerifyStep:
         self.kv_indptr = torch.empty(B + 1, dtype=torch.int32, device=dev)
         self.mask_indptr = torch.empty(B + 1, dtype=torch.int64, device=dev)
         self.mask = torch.empty(sum(n * l for n, l in zip(w.tree_sizes, L)), dtype=torch.uint8, device=dev)
+        # the bit form of the mask (rows of ceil(L/32) uint32 words, held as int32)
+        self.mask_word_indptr = torch.empty(B + 1, dtype=torch.int64, device=dev)
+        self.mask_words = torch.empty(sum(n * ((l + 31) // 32) for n, l in zip(w.tree_sizes, L)),
+                                      dtype=torch.int32, device=dev)
         self.out = torch.empty((T, w.heads, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((T, w.heads), dtype=torch.float32, device=dev)
         nbytes = abi.mla_tree_verify_workspace_bytes(B, T, w.heads, max_splits)
@@ -60,11 +66,24 @@ class VerifyStep:
         abi.mla_tree_draft_kv_scatter(self.draft_kv, self.out_cache_loc, self.pool, self.status, stream)
         abi.mla_tree_kv_indices_build(self.prefix_indices, self.prefix_indptr, self.out_cache_loc,
                                       self.qo_indptr, self.kv_indices, self.kv_indptr, self.status, stream)
-        abi.tree_mask_pack(self.parents, self.qo_indptr, self.kv_indptr, self.mask_indptr, self.mask,
-                           self.status, stream)
+        self.pack_mask(stream)
         self.verify(stream)
 
+    def pack_mask(self, stream=None):
+        if self.mask_bits:
+            abi.tree_mask_pack_bits(self.parents, self.qo_indptr, self.kv_indptr, self.mask_word_indptr,
+                                    self.mask_words, self.status, stream)
+        else:
+            abi.tree_mask_pack(self.parents, self.qo_indptr, self.kv_indptr, self.mask_indptr,
+                               self.mask, self.status, stream)
+
     def verify(self, stream=None):
+        if self.mask_bits:
+            abi.mla_tree_verify_bits(self.q, self.pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
+                                     self.mask_words, self.mask_word_indptr, self.sm_scale, self.out,
+                                     self.lse, self.workspace, self.max_splits, self.path, self.status,
+                                     stream)
+            return
         abi.mla_tree_verify(self.q, self.pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
                             self.mask, self.mask_indptr, self.sm_scale, self.out, self.lse,
                             self.workspace, self.max_splits, self.path, self.status, stream)

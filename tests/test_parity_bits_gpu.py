@@ -1,0 +1,120 @@
+"""GPU parity of the bit-form tree mask (tree_mask_pack_bits,
+mla_tree_verify_bits) through the C ABI: the words bit for bit against the
+fp64 oracle, attention within the verify tolerances, and the same outputs as
+the byte-mask call bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import oracle
+from speculative_decode_mla_tree_gb300 import abi, workloads as W
+from speculative_decode_mla_tree_gb300.step import VerifyStep
+
+from parity import OracleRun, compare_attention, sample_rows
+
+pytestmark = pytest.mark.gpu
+PATHS = [pytest.param(abi.PATH_SIMT, id="simt"), pytest.param(abi.PATH_TC, id="tcgen05")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    __graft_entry__.build()
+
+
+def _edge_workload():
+    parents = [[-1], list(range(-1, 63)), [-1] + [0] * 15, [-1, -1, 0, 2, 1, -1, 5, 3, 3, -1],
+               [-1, 0, 1]]
+    return W.make_workload("edges", 8, [7, 100, 33, 500, 0], None, None, 8192, seed=77,
+                           parents=parents)
+
+
+def _check_words(st, ref_kv_indptr):
+    w = st.w
+    bi, words = oracle.tree_mask_pack_bits(w.parents, w.qo_indptr, ref_kv_indptr)
+    assert int(st.status.item()) == 0
+    assert (st.mask_word_indptr.cpu().numpy() == bi).all()
+    assert (st.mask_words.cpu().numpy().view(np.uint32) == words).all()
+
+
+@pytest.mark.parametrize("cid", ["small", "edges", 2, 4, 5])
+def test_mask_words_bit_exact(cid):
+    w = {"small": lambda: W.small(seed=1), "edges": _edge_workload}.get(cid, lambda: W.config(cid))()
+    st = VerifyStep(w, path=abi.PATH_TC, mask_bits=True)
+    st.load(w)
+    abi.mla_tree_kv_indices_build(st.prefix_indices, st.prefix_indptr, st.out_cache_loc, st.qo_indptr,
+                                  st.kv_indices, st.kv_indptr, st.status)
+    st.pack_mask(); torch.cuda.synchronize()
+    _, kv_indptr = oracle.kv_indices_build(w.prefix_indices, w.prefix_indptr, w.out_cache_loc, w.qo_indptr)
+    _check_words(st, kv_indptr)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wl", ["small", "edges", "c2"])
+def test_bits_attention_full(wl, path):
+    w = {"small": lambda: W.small(seed=1), "edges": _edge_workload, "c2": lambda: W.config(2)}[wl]()
+    st = VerifyStep(w, path=path, mask_bits=True); st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    ref = OracleRun(w)
+    out, lse = ref.attention()
+    compare_attention(st.out, st.lse, out, lse)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bits_equal_bytes(path):
+    """Same kernel, same inputs, mask in either form: identical outputs."""
+    w = W.config(2)
+    a = VerifyStep(w, path=path); a.run()
+    b = VerifyStep(w, path=path, mask_bits=True, pool=a.pool); b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out)
+    assert torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("splits", [1, 7, 64])
+def test_bits_forced_splits_tc(splits):
+    w = W.make_workload("splits", 16, [3000, 20000], "uniform", [32, 8], 65536, seed=5)
+    st = VerifyStep(w, path=abi.PATH_TC, max_splits=splits, mask_bits=True); st.run()
+    torch.cuda.synchronize()
+    ref = OracleRun(w)
+    rows = sample_rows(w, 12, seed=2)
+    out, lse = ref.attention(rows=rows)
+    compare_attention(st.out, st.lse, out, lse, rows=rows)
+
+
+@pytest.mark.parametrize("cid", [3, 4, 5])
+def test_bits_config_sampled_tc(cid):
+    w = W.config(cid)
+    st = VerifyStep(w, path=abi.PATH_TC, mask_bits=True); st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    ref = OracleRun(w)
+    rows = sample_rows(w, 6, seed=cid)
+    out, lse = ref.attention(rows=rows)
+    compare_attention(st.out, st.lse, out, lse, rows=rows)
+
+
+def test_bits_graph_capture_and_replay():
+    w1 = W.make_workload("g", 8, [300, 1200, 77], "uniform", [16, 9, 30], 16384, seed=101)
+    w2 = W.make_workload("g", 8, [300, 1200, 77], "uniform", [16, 9, 30], 16384, seed=202)
+    st = VerifyStep(w1, path=abi.PATH_TC, mask_bits=True)
+    st.run(); torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        st.run()
+    for w in (w1, w2):
+        st.pool.copy_(w.dense_pool("cuda"))
+        st.load(w)
+        g.replay(); torch.cuda.synchronize()
+        ref = OracleRun(w)
+        out, lse = ref.attention()
+        compare_attention(st.out, st.lse, out, lse)
+
+
+def test_bits_capacity_overflow_is_flagged():
+    w = W.small(seed=10)
+    st = VerifyStep(w, mask_bits=True)
+    st.mask_words = st.mask_words[: st.mask_words.numel() // 2]
+    st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) & abi.DEV_BAD_INDPTR

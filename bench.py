@@ -3,22 +3,25 @@
 
 A step is one pass of the whole verify path over one batch: draft-KV scatter,
 KV index marshaling, tree-mask packing and tree-verify attention (with its
-split merge). The tree mask is packed in its bit form by default (one bit
-per (row, column); --mask bytes uses one byte per element). Default workload: 8 requests, prefixes U{1024..4096},
-16-node draft trees (branching <= 3), 8 heads, 65536-slot pool.
+split merge). By default the three marshaling steps run as one launch
+(mla_tree_prepare, which packs the mask in its bit form: one bit per (row,
+column)) ahead of mla_tree_verify_bits; --marshal separate --mask bytes runs
+the four separate calls with the byte mask. Default workload: 8 requests,
+prefixes U{1024..4096}, 16-node draft trees (branching <= 3), 8 heads,
+65536-slot pool.
 
-Timing: each of the four calls is captured once as a CUDA graph; a timed
-step replays the four graphs with CUDA events between them on the launching
-stream, so the step time and the verify call's own time come from the same
-events. L2 is flushed between steps by writing a 256 MiB buffer (outside the
-events): the buffer is written and then read back, so L2 holds only clean
-lines of it and the timed reads pay no write-backs. Inputs are resident in
-HBM when the timed region starts.
+Timing: each call is captured once as a CUDA graph; a timed step replays the
+graphs with CUDA events between them on the launching stream, so the step
+time and the verify call's own time come from the same events. L2 is flushed
+between steps by writing a 256 MiB buffer (outside the events): the buffer is
+written and then read back, so L2 holds only clean lines of it and the timed
+reads pay no write-backs. Inputs are resident in HBM when the timed region
+starts.
 
 value = KV bytes the steps had to read (every prefix + draft row of every
 request once, 1152 B per row) / device time, summed over ranks / max time.
 e2e = the same metric through the public API with host buffers: pinned
-host -> device copies of the step's inputs, the four calls, and the device
+host -> device copies of the step's inputs, the step's calls, and the device
 -> host read of out and lse, all inside the timed region.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
@@ -249,7 +252,11 @@ def run_ours(args):
     __graft_entry__.build()
 
     w = W.config(args.config)
-    st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path, mask_bits=args.mask == "bits")
+    fused = args.marshal == "fused"
+    if fused and args.mask != "bits":
+        raise SystemExit("--marshal fused packs the mask in its bit form: use --mask bits")
+    st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path, mask_bits=args.mask == "bits",
+                    fused=fused)
     stream = torch.cuda.Stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
@@ -264,11 +271,18 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0, "device status %d" % int(st.status.item())
 
-    calls = [lambda: abi.mla_tree_draft_kv_scatter(st.draft_kv, st.out_cache_loc, st.pool, st.status),
-             lambda: abi.mla_tree_kv_indices_build(st.prefix_indices, st.prefix_indptr, st.out_cache_loc,
-                                                   st.qo_indptr, st.kv_indices, st.kv_indptr, st.status),
-             lambda: st.pack_mask(),
-             lambda: st.verify()]
+    if fused:
+        names = ["prepare", "verify"]
+        calls = [lambda: st.prepare(), lambda: st.verify()]
+    else:
+        names = ["scatter", "kv_indices", "mask_pack", "verify"]
+        calls = [lambda: abi.mla_tree_draft_kv_scatter(st.draft_kv, st.out_cache_loc, st.pool, st.status),
+                 lambda: abi.mla_tree_kv_indices_build(st.prefix_indices, st.prefix_indptr,
+                                                       st.out_cache_loc, st.qo_indptr, st.kv_indices,
+                                                       st.kv_indptr, st.status),
+                 lambda: st.pack_mask(),
+                 lambda: st.verify()]
+    ncalls = len(calls)
     graphs = []
     for c in calls:
         g = torch.cuda.CUDAGraph()
@@ -286,13 +300,13 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush_l2(1.0)
-            step([torch.cuda.Event(enable_timing=True) for _ in range(5)])
+            step([torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)])
     torch.cuda.synchronize()
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     idx = vis.split(",")[local] if vis and vis.split(",")[local].strip().isdigit() else str(local)
     clocks = ClockSampler(idx)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)] for _ in range(args.steps)]
     clocks.start()
     time.sleep(0.3)
     if world > 1:
@@ -307,22 +321,22 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
 
-    step_ms = [e[0].elapsed_time(e[4]) for e in events]
-    call_ms = [[e[i].elapsed_time(e[i + 1]) for e in events] for i in range(4)]
+    step_ms = [e[0].elapsed_time(e[ncalls]) for e in events]
+    call_ms = [[e[i].elapsed_time(e[i + 1]) for e in events] for i in range(ncalls)]
     total_ms = max_over_ranks(sum(step_ms), dev)
     assert int(st.status.item()) == 0
 
     kv_bytes = w.kv_bytes()
     value = whole_job_gbs(world, args.steps, kv_bytes, total_ms)
     byts, flops = alg_cost(w, args.mask == "bits")
-    verify_ms = statistics.mean(call_ms[3])
+    verify_ms = statistics.mean(call_ms[-1])
     hbm, tf_burst, tf_sus, which = _peaks()
     achieved_gbs = byts / (verify_ms * 1e-3) / 1e9
     achieved_tf = flops / (verify_ms * 1e-3) / 1e12
     t_hbm, t_tc = byts / (hbm * 1e9), flops / (tf_burst * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     launches_verify = abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, args.max_splits, args.path)
-    launches = args.steps * (3 + launches_verify)
+    launches = args.steps * (ncalls - 1 + launches_verify)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -367,13 +381,12 @@ def run_ours(args):
             "config": {"workload": W.CONFIG_NAMES[args.config], "batch": w.batch, "heads": w.heads,
                        "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
                        "path": ["auto", "simt", "tensor-core"][args.path],
-                       "max_splits": args.max_splits, "mask": args.mask,
+                       "max_splits": args.max_splits, "mask": args.mask, "marshal": args.marshal,
                        "l2": "flushed between steps: 256 MiB written then read back, outside the events",
                        "timing": "per-call CUDA graphs, CUDA events on the launching stream"},
-            "step_ms": {"scatter": statistics.mean(call_ms[0]), "kv_indices": statistics.mean(call_ms[1]),
-                        "mask_pack": statistics.mean(call_ms[2]), "verify": verify_ms,
-                        "verify_p10": sorted(call_ms[3])[len(call_ms[3]) // 10],
-                        "verify_p90": sorted(call_ms[3])[(9 * len(call_ms[3])) // 10]},
+            "step_ms": dict([(nm, statistics.mean(c)) for nm, c in zip(names, call_ms)] +
+                            [("verify_p10", sorted(call_ms[-1])[len(call_ms[-1]) // 10]),
+                             ("verify_p90", sorted(call_ms[-1])[(9 * len(call_ms[-1])) // 10])]),
             "roofline": {"kernel": "mla_tree_verify (all launches of the call)", "bound": bound,
                          "achieved": achieved_gbs if bound == "hbm" else achieved_tf,
                          "peak": hbm if bound == "hbm" else tf_burst,
@@ -402,6 +415,8 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--marshal", default="fused", choices=["fused", "separate"],
+                    help="scatter, index marshaling and mask packing as one launch or three")
     ap.add_argument("--mask", default="bits", choices=["bytes", "bits"],
                     help="tree-mask form: one byte or one bit per (row, column)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -160,6 +160,28 @@ int tree_mask_pack_bits(const int32_t* parents, const int32_t* qo_indptr, const 
                         int32_t* dev_status, mt_stream_t stream);
 
 /*
+ * The three marshaling steps of one verify step in one launch: exactly the
+ * effect of mla_tree_draft_kv_scatter(draft_kv, ...), then
+ * mla_tree_kv_indices_build(...) and tree_mask_pack_bits(...) with the
+ * kv_indptr it writes, on the same arguments (see those entry points for
+ * layouts, capacities and the status bits they set). The three parts run
+ * side by side; the mask part takes each request's key count from
+ * prefix_indptr and qo_indptr instead of reading kv_indptr. draft_kv and
+ * kv_buf must be 16-byte aligned and draft_row_stride a multiple of 8
+ * elements, else MT_EINVAL (the separate entry points take any alignment).
+ * The paper's integration runs these steps in Python inside the serving
+ * engine; here they are one kernel ahead of mla_tree_verify_bits.
+ */
+int mla_tree_prepare(const mt_bf16* draft_kv, int64_t draft_row_stride,
+                     const int32_t* out_cache_loc, const int32_t* prefix_indices,
+                     int64_t prefix_indices_len, const int32_t* prefix_indptr,
+                     const int32_t* qo_indptr, const int32_t* parents, int batch, int total_q,
+                     mt_bf16* kv_buf, int64_t num_slots,
+                     int32_t* kv_indices, int64_t kv_indices_capacity, int32_t* kv_indptr,
+                     int64_t* mask_word_indptr, uint32_t* mask_words, int64_t mask_capacity_words,
+                     int32_t* dev_status, mt_stream_t stream);
+
+/*
  * Bytes of scratch workspace mla_tree_verify needs for these capacities
  * (max_splits 0 = the automatic choice mla_tree_verify makes for 0).
  * Holds per-split partial outputs (fp32 [splits][total_q*heads][512]), their

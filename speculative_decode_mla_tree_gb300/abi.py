@@ -17,7 +17,7 @@ DEV_BAD_SLOT, DEV_BAD_PARENT, DEV_BAD_INDPTR, DEV_TREE_TOO_BIG, DEV_TIMEOUT = 1,
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 
 EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_scatter",
-           "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits",
+           "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits", "mla_tree_prepare",
            "mla_tree_verify_workspace_bytes", "mla_tree_verify_launch_count", "mla_tree_verify",
            "mla_tree_verify_bits", "mla_tree_verify_noalloc"]
 MT_ESCRATCH = -5
@@ -51,6 +51,9 @@ def load():
     lib.tree_mask_pack.argtypes = [P, P, P, I32, I32, P, P, I64, P, P]
     lib.tree_mask_pack_bits.restype = I32
     lib.tree_mask_pack_bits.argtypes = [P, P, P, I32, I32, P, P, I64, P, P]
+    lib.mla_tree_prepare.restype = I32
+    lib.mla_tree_prepare.argtypes = [P, I64, P, P, I64, P, P, P, I32, I32, P, I64, P, I64, P, P, P, I64,
+                                     P, P]
     lib.mla_tree_verify_workspace_bytes.restype = SZ
     lib.mla_tree_verify_workspace_bytes.argtypes = [I32, I32, I32, I32]
     lib.mla_tree_verify_launch_count.restype = I32
@@ -142,6 +145,29 @@ def tree_mask_pack_bits(parents, qo_indptr, kv_indptr, mask_word_indptr, mask_wo
         _ptr(mask_words, torch.int32, "mask_words"), mask_words.numel(),
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "tree_mask_pack_bits")
+
+
+def mla_tree_prepare(draft_kv, out_cache_loc, prefix_indices, prefix_indptr, qo_indptr, parents,
+                     kv_buf, kv_indices, kv_indptr, mask_word_indptr, mask_words, status=None,
+                     stream=None):
+    """Draft-KV scatter, KV index marshaling and bit-form mask packing in one launch."""
+    if (draft_kv.dim() != 2 or draft_kv.stride(1) != 1 or draft_kv.dtype != torch.bfloat16
+            or not draft_kv.is_cuda):
+        raise MlaTreeError("draft_kv must be a CUDA bf16 [T, >=576] tensor with unit column stride")
+    batch = qo_indptr.numel() - 1
+    rc = load().mla_tree_prepare(
+        draft_kv.data_ptr() if draft_kv.numel() else None, draft_kv.stride(0),
+        _ptr(out_cache_loc, torch.int32, "out_cache_loc"),
+        _ptr(prefix_indices, torch.int32, "prefix_indices"), prefix_indices.numel(),
+        _ptr(prefix_indptr, torch.int32, "prefix_indptr"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(parents, torch.int32, "parents"), batch, out_cache_loc.numel(),
+        _ptr(kv_buf, torch.bfloat16, "kv_buf"), kv_buf.shape[0],
+        _ptr(kv_indices, torch.int32, "kv_indices"), kv_indices.numel(),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"),
+        _ptr(mask_word_indptr, torch.int64, "mask_word_indptr"),
+        _ptr(mask_words, torch.int32, "mask_words"), mask_words.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "mla_tree_prepare")
 
 
 def mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits=0):

@@ -133,6 +133,32 @@ int tree_mask_pack_bits(const int32_t* parents, const int32_t* qo_indptr, const 
                                                 dev_status, sm_count(), (cudaStream_t)stream));
 }
 
+int mla_tree_prepare(const mt_bf16* draft_kv, int64_t draft_row_stride,
+                     const int32_t* out_cache_loc, const int32_t* prefix_indices,
+                     int64_t prefix_indices_len, const int32_t* prefix_indptr,
+                     const int32_t* qo_indptr, const int32_t* parents, int batch, int total_q,
+                     mt_bf16* kv_buf, int64_t num_slots, int32_t* kv_indices,
+                     int64_t kv_indices_capacity, int32_t* kv_indptr, int64_t* mask_word_indptr,
+                     uint32_t* mask_words, int64_t mask_capacity_words, int32_t* dev_status,
+                     mt_stream_t stream) {
+  if (batch < 0 || total_q < 0 || num_slots < 0 || kv_indices_capacity < 0 ||
+      prefix_indices_len < 0 || mask_capacity_words < 0 || draft_row_stride < MT_D_QK)
+    return MT_EINVAL;
+  if (batch == 0) return MT_OK;
+  if (!prefix_indptr || !qo_indptr || !kv_indptr || !mask_word_indptr || !kv_buf) return MT_EINVAL;
+  if (total_q > 0 && (!draft_kv || !out_cache_loc || !parents)) return MT_EINVAL;
+  if (kv_indices_capacity > 0 && !kv_indices) return MT_EINVAL;
+  if (prefix_indices_len > 0 && !prefix_indices) return MT_EINVAL;
+  if (mask_capacity_words > 0 && !mask_words) return MT_EINVAL;
+  if ((uintptr_t)draft_kv % 16 || (uintptr_t)kv_buf % 16 || draft_row_stride % 8) return MT_EINVAL;
+  if (batch > 65535) return MT_EUNSUPPORTED;
+  return cuda_status(launch_prepare(draft_kv, draft_row_stride, out_cache_loc, prefix_indices,
+                                    prefix_indices_len, prefix_indptr, qo_indptr, parents, batch,
+                                    total_q, kv_buf, num_slots, kv_indices, kv_indices_capacity,
+                                    kv_indptr, mask_word_indptr, mask_words, mask_capacity_words,
+                                    dev_status, sm_count(), (cudaStream_t)stream));
+}
+
 size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int max_splits) {
   if (batch < 0 || total_q < 0 || heads < 0 || max_splits < 0 || max_splits > MT_MAX_SPLITS) return 0;
   if (max_splits == 0) max_splits = auto_max_splits(batch, total_q, heads, sm_count());

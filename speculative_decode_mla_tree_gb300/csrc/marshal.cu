@@ -15,15 +15,14 @@ namespace mt {
 // ---------------------------------------------------------------- scatter
 
 // One thread per 16-byte vector of a 1152-byte row: a warp moves 512
-// contiguous bytes of one source row into one pool row.
-__global__ void __launch_bounds__(256) draft_kv_scatter_vec(const uint4* __restrict__ src,
-                                                            int64_t src_stride_vec,
-                                                            const int32_t* __restrict__ loc,
-                                                            int total_q, uint4* __restrict__ kv,
-                                                            int64_t num_slots, int32_t* status) {
+// contiguous bytes of one source row into one pool row. Block bid of nb
+// blocks of 256 threads.
+__device__ __forceinline__ void scatter_vec_body(const uint4* __restrict__ src, int64_t src_stride_vec,
+                                                 const int32_t* __restrict__ loc, int total_q,
+                                                 uint4* __restrict__ kv, int64_t num_slots,
+                                                 int32_t* status, int64_t bid, int64_t nb) {
   const int64_t total = (int64_t)total_q * kRowVec;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t idx = bid * 256 + threadIdx.x; idx < total; idx += nb * 256) {
     const int64_t t = idx / kRowVec;
     const int v = (int)(idx - t * kRowVec);
     const int32_t slot = loc[t];
@@ -33,6 +32,14 @@ __global__ void __launch_bounds__(256) draft_kv_scatter_vec(const uint4* __restr
     }
     kv[(int64_t)slot * kRowVec + v] = src[t * src_stride_vec + v];
   }
+}
+
+__global__ void __launch_bounds__(256) draft_kv_scatter_vec(const uint4* __restrict__ src,
+                                                            int64_t src_stride_vec,
+                                                            const int32_t* __restrict__ loc,
+                                                            int total_q, uint4* __restrict__ kv,
+                                                            int64_t num_slots, int32_t* status) {
+  scatter_vec_body(src, src_stride_vec, loc, total_q, kv, num_slots, status, blockIdx.x, gridDim.x);
 }
 
 // Fallback for sources that are not 16-byte aligned: 2-byte copies.
@@ -75,19 +82,18 @@ cudaError_t launch_draft_kv_scatter(const uint16_t* src, int64_t src_stride, con
 
 // ---------------------------------------------------------------- kv indices
 
-// grid (chunks, batch): chunk c of request b copies positions j = c*256+tid,
-// stepping by chunks*256.
-__global__ void __launch_bounds__(256) kv_indices_build_kernel(
+// Chunk c of request b (of `chunks`, 256 threads each) copies positions
+// j = c*256+tid, stepping by chunks*256.
+__device__ __forceinline__ void indices_body(
     const int32_t* __restrict__ pidx, int64_t pidx_len, const int32_t* __restrict__ pptr,
     const int32_t* __restrict__ loc, const int32_t* __restrict__ qptr, int batch, int total_q,
     int32_t* __restrict__ kv_indices, int64_t capacity, int32_t* __restrict__ kv_indptr,
-    int32_t* status) {
-  const int b = blockIdx.y;
+    int32_t* status, int b, int c, int chunks) {
   const int64_t p0 = pptr[b], p1 = pptr[b + 1];
   const int64_t q0 = qptr[b], q1 = qptr[b + 1];
   const int64_t base = p0 + q0;
   const int64_t P = p1 - p0, n = q1 - q0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (c == 0 && threadIdx.x == 0) {
     kv_indptr[b] = (int32_t)base;
     if (b == batch - 1) {
       kv_indptr[batch] = (int32_t)(p1 + q1);
@@ -96,13 +102,22 @@ __global__ void __launch_bounds__(256) kv_indices_build_kernel(
   }
   if (P < 0 || n < 0 || p0 < 0 || q0 < 0 || p1 > pidx_len || q1 > total_q ||
       base + P + n > capacity || base + P + n > 0x7fffffffLL) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
+    if (c == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
     return;
   }
   const int64_t L = P + n;
-  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < L;
-       j += (int64_t)gridDim.x * blockDim.x)
+  for (int64_t j = (int64_t)c * 256 + threadIdx.x; j < L; j += (int64_t)chunks * 256)
     kv_indices[base + j] = j < P ? pidx[p0 + j] : loc[q0 + (j - P)];
+}
+
+// grid (chunks, batch)
+__global__ void __launch_bounds__(256) kv_indices_build_kernel(
+    const int32_t* __restrict__ pidx, int64_t pidx_len, const int32_t* __restrict__ pptr,
+    const int32_t* __restrict__ loc, const int32_t* __restrict__ qptr, int batch, int total_q,
+    int32_t* __restrict__ kv_indices, int64_t capacity, int32_t* __restrict__ kv_indptr,
+    int32_t* status) {
+  indices_body(pidx, pidx_len, pptr, loc, qptr, batch, total_q, kv_indices, capacity, kv_indptr,
+               status, blockIdx.y, blockIdx.x, gridDim.x);
 }
 
 cudaError_t launch_kv_indices_build(const int32_t* pidx, int64_t pidx_len, const int32_t* pptr,
@@ -253,31 +268,40 @@ cudaError_t launch_tree_mask_pack(const int32_t* parents, const int32_t* qptr, c
 // W = ceil(L / 32) words, column j in bit j % 32 of word j / 32. Words wholly
 // inside the prefix are all ones; only the few words that reach the draft
 // columns read the row's ancestor set.
-__global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_bits_kernel(
+// Key positions of request r: from kv_indptr when given, else prefix length
+// (prefix_indptr) plus draft nodes (qo_indptr), which is what kv_indptr holds.
+__device__ __forceinline__ long long req_len(const int32_t* kptr, const int32_t* pptr,
+                                             const int32_t* qptr, int r) {
+  if (kptr) return (long long)kptr[r + 1] - kptr[r];
+  return ((long long)pptr[r + 1] - pptr[r]) + ((long long)qptr[r + 1] - qptr[r]);
+}
+
+// Row group g (of `groups`, kMaskThreads threads each) of request b.
+__device__ __forceinline__ void mask_bits_body(
     const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
-    const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ word_indptr,
-    uint32_t* __restrict__ words, int64_t capacity, int32_t* status) {
+    const int32_t* __restrict__ kptr, const int32_t* __restrict__ pptr, int batch, int total_q,
+    int64_t* __restrict__ word_indptr, uint32_t* __restrict__ words, int64_t capacity,
+    int32_t* status, int b, int g, int groups) {
   __shared__ uint32_t bits[MT_MAX_TREE / 32];
   __shared__ long long s_base;
   __shared__ int s_bad;
-  const int b = blockIdx.y;
   if (threadIdx.x == 0) {
     long long base = 0;
     int bad = 0;
     for (int r = 0; r < b; ++r) {
       const long long n = (long long)qptr[r + 1] - qptr[r];
-      const long long L = (long long)kptr[r + 1] - kptr[r];
+      const long long L = req_len(kptr, pptr, qptr, r);
       if (n < 0 || L < n) bad = 1;
       base += n * ((L + 31) >> 5);
     }
     s_base = base;
     s_bad = bad;
-    if (b == 0 && blockIdx.x == 0) {
+    if (b == 0 && g == 0) {
       long long acc = 0;
       word_indptr[0] = 0;
       for (int r = 0; r < batch; ++r) {
         const long long n = (long long)qptr[r + 1] - qptr[r];
-        const long long L = (long long)kptr[r + 1] - kptr[r];
+        const long long L = req_len(kptr, pptr, qptr, r);
         acc += (n >= 0 && L >= n) ? n * ((L + 31) >> 5) : 0;
         word_indptr[r + 1] = acc;
       }
@@ -286,20 +310,20 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_bits_kernel(
   __syncthreads();
   const int64_t q0 = qptr[b];
   const int64_t n = (int64_t)qptr[b + 1] - q0;
-  const int64_t L = (int64_t)kptr[b + 1] - kptr[b];
+  const int64_t L = req_len(kptr, pptr, qptr, b);
   const int64_t P = L - n;
   const int64_t W = (L + 31) >> 5;
   const int64_t base = s_base;
   if (s_bad || n < 0 || P < 0 || q0 < 0 || q0 + n > total_q || base + n * W > capacity) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
+    if (g == 0 && threadIdx.x == 0) flag(status, MT_DEV_BAD_INDPTR);
     return;
   }
   if (n > MT_MAX_TREE) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, MT_DEV_TREE_TOO_BIG);
+    if (g == 0 && threadIdx.x == 0) flag(status, MT_DEV_TREE_TOO_BIG);
     return;
   }
   const int nwords = (int)((n + 31) >> 5);
-  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+  for (int64_t i = g; i < n; i += groups) {
     for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -337,6 +361,70 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_bits_kernel(
     }
     __syncthreads();
   }
+}
+
+// grid (row groups, batch)
+__global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_bits_kernel(
+    const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
+    const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ word_indptr,
+    uint32_t* __restrict__ words, int64_t capacity, int32_t* status) {
+  mask_bits_body(parents, qptr, kptr, nullptr, batch, total_q, word_indptr, words, capacity, status,
+                 blockIdx.y, blockIdx.x, gridDim.x);
+}
+
+// ---------------------------------------------------------------- fused
+
+// The three marshaling steps of one verify step in one launch of 256-thread
+// blocks: blocks [0, ns) scatter the draft rows, the next batch * ni build
+// kv_indices (chunk (k / batch) of request k % batch), the last batch * nm pack
+// the bit-form mask (row group (k / batch) of request k % batch). The mask
+// part takes each request's key count from prefix_indptr and qo_indptr, so
+// it does not wait for the kv_indptr this launch also writes.
+static_assert(kMaskThreads == 256, "one block size for every part of the fused launch");
+__global__ void __launch_bounds__(256) prepare_kernel(
+    const uint4* __restrict__ src, int64_t src_stride_vec, const int32_t* __restrict__ loc,
+    const int32_t* __restrict__ pidx, int64_t pidx_len, const int32_t* __restrict__ pptr,
+    const int32_t* __restrict__ qptr, const int32_t* __restrict__ parents, int batch, int total_q,
+    uint4* __restrict__ kv, int64_t num_slots, int32_t* __restrict__ kv_indices,
+    int64_t kv_capacity, int32_t* __restrict__ kv_indptr, int64_t* __restrict__ word_indptr,
+    uint32_t* __restrict__ words, int64_t word_capacity, int32_t* status, int ns, int ni, int nm) {
+  const int k = blockIdx.x;
+  if (k < ns) {
+    scatter_vec_body(src, src_stride_vec, loc, total_q, kv, num_slots, status, k, ns);
+  } else if (k < ns + batch * ni) {
+    const int r = k - ns;
+    indices_body(pidx, pidx_len, pptr, loc, qptr, batch, total_q, kv_indices, kv_capacity, kv_indptr,
+                 status, r % batch, r / batch, ni);
+  } else {
+    const int r = k - ns - batch * ni;
+    mask_bits_body(parents, qptr, nullptr, pptr, batch, total_q, word_indptr, words, word_capacity,
+                   status, r % batch, r / batch, nm);
+  }
+}
+
+cudaError_t launch_prepare(const uint16_t* src, int64_t src_stride, const int32_t* loc,
+                           const int32_t* pidx, int64_t pidx_len, const int32_t* pptr,
+                           const int32_t* qptr, const int32_t* parents, int batch, int total_q,
+                           uint16_t* kv, int64_t num_slots, int32_t* kv_indices, int64_t kv_capacity,
+                           int32_t* kv_indptr, int64_t* word_indptr, uint32_t* words,
+                           int64_t word_capacity, int32_t* status, int num_sms, cudaStream_t stream) {
+  // same work splits as the separate launches
+  int64_t ns = ((int64_t)total_q * kRowVec + 255) / 256;
+  if (ns > (int64_t)num_sms * 8) ns = (int64_t)num_sms * 8;
+  if (ns < 1) ns = 1;
+  int ni = (2 * num_sms + batch - 1) / batch;
+  if (ni < 1) ni = 1;
+  if (ni > 256) ni = 256;
+  int nm = (2 * num_sms + batch - 1) / batch;
+  if (nm < 1) nm = 1;
+  if (nm > 64) nm = 64;
+  const int64_t blocks = ns + (int64_t)batch * (ni + nm);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prepare_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      (const uint4*)src, src_stride / 8, loc, pidx, pidx_len, pptr, qptr, parents, batch, total_q,
+      (uint4*)kv, num_slots, kv_indices, kv_capacity, kv_indptr, word_indptr, words, word_capacity,
+      status, (int)ns, ni, nm);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tree_mask_pack_bits(const int32_t* parents, const int32_t* qptr,

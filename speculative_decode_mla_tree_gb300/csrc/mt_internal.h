@@ -62,6 +62,14 @@ cudaError_t launch_tree_mask_pack_bits(const int32_t* parents, const int32_t* qp
                                        int64_t* word_indptr, uint32_t* words, int64_t capacity,
                                        int32_t* status, int num_sms, cudaStream_t stream);
 
+// The three marshaling steps in one launch (16-byte aligned draft rows only).
+cudaError_t launch_prepare(const uint16_t* src, int64_t src_stride, const int32_t* loc,
+                           const int32_t* pidx, int64_t pidx_len, const int32_t* pptr,
+                           const int32_t* qptr, const int32_t* parents, int batch, int total_q,
+                           uint16_t* kv, int64_t num_slots, int32_t* kv_indices, int64_t kv_capacity,
+                           int32_t* kv_indptr, int64_t* word_indptr, uint32_t* words,
+                           int64_t word_capacity, int32_t* status, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream);
 // Tensor-core path; returns cudaErrorNotSupported when it cannot serve `a`.

@@ -12,7 +12,10 @@ from . import abi
 
 class VerifyStep:
     def __init__(self, w, device="cuda", max_splits=0, path=abi.PATH_AUTO, pool=None,
-                 mask_bits=False):
+                 mask_bits=False, fused=False):
+        """mask_bits: pack the tree mask in its bit form; fused (implies
+        mask_bits): scatter, index marshaling and mask packing as one launch
+        (mla_tree_prepare)."""
         dev = torch.device(device)
         self.device = dev
         self.w = w
@@ -20,7 +23,8 @@ class VerifyStep:
         self.sm_scale = w.sm_scale
         self.max_splits = max_splits
         self.path = path
-        self.mask_bits = mask_bits
+        self.fused = fused
+        self.mask_bits = mask_bits or fused
         B, T = w.batch, w.total_q
         L = [p + n for p, n in zip(w.prefix_lens, w.tree_sizes)]
         # resident latent-KV pool (before the draft rows are scattered in)
@@ -63,11 +67,20 @@ class VerifyStep:
             d.copy_(h, non_blocking=False)
 
     def run(self, stream=None):
+        if self.fused:
+            self.prepare(stream)
+            self.verify(stream)
+            return
         abi.mla_tree_draft_kv_scatter(self.draft_kv, self.out_cache_loc, self.pool, self.status, stream)
         abi.mla_tree_kv_indices_build(self.prefix_indices, self.prefix_indptr, self.out_cache_loc,
                                       self.qo_indptr, self.kv_indices, self.kv_indptr, self.status, stream)
         self.pack_mask(stream)
         self.verify(stream)
+
+    def prepare(self, stream=None):
+        abi.mla_tree_prepare(self.draft_kv, self.out_cache_loc, self.prefix_indices, self.prefix_indptr,
+                             self.qo_indptr, self.parents, self.pool, self.kv_indices, self.kv_indptr,
+                             self.mask_word_indptr, self.mask_words, self.status, stream)
 
     def pack_mask(self, stream=None):
         if self.mask_bits:

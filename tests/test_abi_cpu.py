@@ -75,6 +75,26 @@ def test_host_argument_checks(lib):
     assert lib.mla_tree_kv_indices_build(null, 0, null, null, null, 2, 4, null, 0, null, null, null) == abi.MT_EINVAL
     assert lib.tree_mask_pack(null, null, null, 0, 0, null, null, 0, null, null) == abi.MT_OK
     assert lib.tree_mask_pack(null, null, null, 1, 3, null, null, 0, null, null) == abi.MT_EINVAL
+    assert lib.tree_mask_pack_bits(null, null, null, 0, 0, null, null, 0, null, null) == abi.MT_OK
+    assert lib.tree_mask_pack_bits(null, null, null, 1, 3, null, null, 0, null, null) == abi.MT_EINVAL
+    # fused marshaling: short row stride, null pointers, misaligned draft rows
+    prep = [fake, 576, fake, fake, 4, fake, fake, fake, 1, 2, fake, 10, fake, 16, fake, fake, fake, 8,
+            null, null]
+    bad = list(prep); bad[1] = 100
+    assert lib.mla_tree_prepare(*bad) == abi.MT_EINVAL
+    bad = list(prep); bad[7] = null
+    assert lib.mla_tree_prepare(*bad) == abi.MT_EINVAL
+    bad = list(prep); bad[0] = fake + 8
+    assert lib.mla_tree_prepare(*bad) == abi.MT_EINVAL
+    bad = list(prep); bad[1] = 580
+    assert lib.mla_tree_prepare(*bad) == abi.MT_EINVAL
+    bad = list(prep); bad[8] = 0
+    assert lib.mla_tree_prepare(*bad) == abi.MT_OK
+    # bit-form verify shares the verify checks
+    args3 = list(args2); args3[16] = fake; args3[17] = 16
+    assert lib.mla_tree_verify_bits(*args3) == abi.MT_EWORKSPACE
+    args3[12] = 0
+    assert lib.mla_tree_verify_bits(*args3) == abi.MT_EINVAL
 
 
 def test_workspace_size_grows_with_splits(lib):

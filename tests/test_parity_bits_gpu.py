@@ -118,3 +118,51 @@ def test_bits_capacity_overflow_is_flagged():
     st.mask_words = st.mask_words[: st.mask_words.numel() // 2]
     st.run(); torch.cuda.synchronize()
     assert int(st.status.item()) & abi.DEV_BAD_INDPTR
+
+
+@pytest.mark.parametrize("wl", ["small", "edges", "c2", "c4"])
+def test_prepare_matches_separate_calls(wl):
+    """mla_tree_prepare writes exactly what the three separate entry points
+    write (pool rows, kv_indices, kv_indptr, mask words and offsets), and
+    those match the oracle."""
+    w = {"small": lambda: W.small(seed=1), "edges": _edge_workload, "c2": lambda: W.config(2),
+         "c4": lambda: W.config(4)}[wl]()
+    a = VerifyStep(w, path=abi.PATH_TC, mask_bits=True)
+    a.load(w)
+    abi.mla_tree_draft_kv_scatter(a.draft_kv, a.out_cache_loc, a.pool, a.status)
+    abi.mla_tree_kv_indices_build(a.prefix_indices, a.prefix_indptr, a.out_cache_loc, a.qo_indptr,
+                                  a.kv_indices, a.kv_indptr, a.status)
+    a.pack_mask()
+    b = VerifyStep(w, path=abi.PATH_TC, fused=True)
+    b.load(w)
+    b.prepare()
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    for x, y in [(a.pool, b.pool), (a.kv_indices, b.kv_indices), (a.kv_indptr, b.kv_indptr),
+                 (a.mask_word_indptr, b.mask_word_indptr), (a.mask_words, b.mask_words)]:
+        assert torch.equal(x, y)
+    kv_indices, kv_indptr = oracle.kv_indices_build(w.prefix_indices, w.prefix_indptr, w.out_cache_loc,
+                                                    w.qo_indptr)
+    assert (b.kv_indices.cpu().numpy() == kv_indices).all()
+    _check_words(b, kv_indptr)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_fused_step_attention(path):
+    w = W.config(2)
+    st = VerifyStep(w, path=path, fused=True); st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    ref = OracleRun(w)
+    out, lse = ref.attention()
+    compare_attention(st.out, st.lse, out, lse)
+
+
+def test_prepare_flags_bad_slot_and_parent():
+    w = W.small(seed=12)
+    st = VerifyStep(w, fused=True)
+    st.load(w)
+    st.out_cache_loc[1] = w.num_slots + 3
+    st.parents[2] = 7
+    st.prepare(); torch.cuda.synchronize()
+    s = int(st.status.item())
+    assert s & abi.DEV_BAD_SLOT and s & abi.DEV_BAD_PARENT

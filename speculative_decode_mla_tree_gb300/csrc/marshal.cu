@@ -195,6 +195,14 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
     return;
   }
   const int words = (int)((n + 31) >> 5);
+  // the request's parent array, staged once (-2: out of range)
+  __shared__ int16_t par_s[MT_MAX_TREE];
+  if (blockIdx.x < n) {
+    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
+      const int32_t p = parents[q0 + k];
+      par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);
+    }
+  }
   for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
     for (int w = threadIdx.x; w < words; w += blockDim.x) bits[w] = 0u;
     __syncthreads();
@@ -203,8 +211,8 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
       int64_t k = i;
       while (k >= 0) {
         bits[k >> 5] |= 1u << (k & 31);
-        const int32_t p = parents[q0 + k];
-        if (p < -1 || p >= k) {
+        const int p = par_s[k];
+        if (p == -2) {
           flag(status, MT_DEV_BAD_PARENT);
           break;
         }
@@ -323,6 +331,15 @@ __device__ __forceinline__ void mask_bits_body(
     return;
   }
   const int nwords = (int)((n + 31) >> 5);
+  // the request's parent array, staged once (the walks below would otherwise
+  // be a chain of dependent global loads, one per tree level)
+  __shared__ int16_t par_s[MT_MAX_TREE];
+  if (g < n) {
+    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
+      const int32_t p = parents[q0 + k];
+      par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);  // -2: out of range
+    }
+  }
   for (int64_t i = g; i < n; i += groups) {
     for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
     __syncthreads();
@@ -331,8 +348,8 @@ __device__ __forceinline__ void mask_bits_body(
       int64_t k = i;
       while (k >= 0) {
         bits[k >> 5] |= 1u << (k & 31);
-        const int32_t p = parents[q0 + k];
-        if (p < -1 || p >= k) {
+        const int p = par_s[k];
+        if (p == -2) {
           flag(status, MT_DEV_BAD_PARENT);
           break;
         }
@@ -388,6 +405,9 @@ __global__ void __launch_bounds__(256) prepare_kernel(
     uint4* __restrict__ kv, int64_t num_slots, int32_t* __restrict__ kv_indices,
     int64_t kv_capacity, int32_t* __restrict__ kv_indptr, int64_t* __restrict__ word_indptr,
     uint32_t* __restrict__ words, int64_t word_capacity, int32_t* status, int ns, int ni, int nm) {
+  // the verify kernel that follows may be scheduled now; it waits for this
+  // grid to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int k = blockIdx.x;
   if (k < ns) {
     scatter_vec_body(src, src_stride_vec, loc, total_q, kv, num_slots, status, k, ns);

@@ -49,6 +49,9 @@ __device__ __forceinline__ void load_row18(const uint16_t* row, int lane, float 
 }
 
 __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyArgs a) {
+  // launched as a programmatic dependent of the previous kernel in the
+  // stream: wait for it to complete before reading anything it may write
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int hg_count = (a.heads + kRows - 1) / kRows;
@@ -166,9 +169,16 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
   const int hg_count = (a.heads + kRows - 1) / kRows;
   const int64_t warps = (int64_t)a.total_q * hg_count;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
-  dim3 grid((unsigned)blocks, (unsigned)a.max_splits);
-  verify_simt_kernel<<<grid, kWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, (unsigned)a.max_splits);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_simt_kernel, a);
 }
 
 // ---------------------------------------------------------------- merge

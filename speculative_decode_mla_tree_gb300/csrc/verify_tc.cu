@@ -355,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // the last CTA publishes the split counts: with fewer items than clusters it
   // has none of its own, so the extra stores delay no item
+  // Launched as a programmatic dependent of the kernel before it (the
+  // marshaling of the same step): the set-up above overlaps that kernel's
+  // tail; nothing it writes is read before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == 0)
     build_plan(a, p.nclusters, plan, ord, obase, total_items_s, lane, blockIdx.x == gridDim.x - 1);
   tc_fence_before();
@@ -1035,13 +1039,17 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel in the stream finishes (the kernel
+  // waits for it before reading anything)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   cudaError_t e = a.bits_mask
       ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, p, tq_rope, tkv_lat, tkv_rope)
       : cudaLaunchKernelEx(&cfg, verify_tc_kernel<false>, p, tq_rope, tkv_lat, tkv_rope);

@@ -24,7 +24,7 @@ namespace mt {
 
 constexpr int kRows = 4;          // heads per warp
 constexpr int kWarps = 4;         // warps per CTA
-constexpr int kMinChunk = 256;    // smallest KV split worth a warp
+constexpr int kMinChunk = 8;      // smallest KV split worth a warp (keys are a serial latency chain)
 
 __device__ __forceinline__ int simt_splits(int L, int max_splits, int* chunk) {
   int c = (L + max_splits - 1) / max_splits;

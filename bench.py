@@ -254,7 +254,7 @@ def run_ours(args):
         dist.barrier()
     __graft_entry__.build()
 
-    w = W.config(args.config)
+    w = W.config(args.config, args.kv_layout)
     fused = args.marshal == "fused"
     if fused and args.mask != "bits":
         raise SystemExit("--marshal fused packs the mask in its bit form: use --mask bits")
@@ -404,6 +404,7 @@ def run_ours(args):
                        "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
                        "path": ["auto", "simt", "tensor-core"][args.path],
                        "max_splits": args.max_splits, "mask": args.mask, "marshal": args.marshal,
+                       "kv_layout": args.kv_layout,
                        "l2": "flushed between steps: 256 MiB written then read back, outside the events",
                        "timing": "whole step as one CUDA graph (value, ms_per_step); per-call graphs "
                                  "(us_per_call, step_ms); CUDA events on the launching stream"},
@@ -438,6 +439,9 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--kv-layout", default="shuffled", choices=["shuffled", "contiguous", "paged64"],
+                    help="how pool slots are handed out: shuffled (the workloads' default), one "
+                         "contiguous run, or random 64-slot pages")
     ap.add_argument("--marshal", default="fused", choices=["fused", "separate"],
                     help="scatter, index marshaling and mask packing as one launch or three")
     ap.add_argument("--mask", default="bits", choices=["bytes", "bits"],

@@ -65,6 +65,7 @@ enum {
                                      qo_indptr[batch] != total_q */
 #define MT_DEV_TREE_TOO_BIG 0x08  /* a request with more than MT_MAX_TREE draft nodes */
 #define MT_DEV_TIMEOUT      0x10  /* a bounded wait inside a kernel gave up */
+#define MT_DEV_MISMATCH     0x20  /* validate mode: the two kernels disagree beyond the tolerance */
 
 #define MT_D_QK 576
 #define MT_D_V 512
@@ -248,6 +249,34 @@ int mla_tree_verify_bits(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
                          mt_bf16* out, float* lse,
                          void* workspace, size_t workspace_bytes, int max_splits, int path,
                          int32_t* dev_status, mt_stream_t stream);
+
+/*
+ * Validate mode ("Deploying a Custom sm_120 Verify Kernel into Production",
+ * "The Validate Mode": the custom kernel runs next to the reference path on
+ * the same tensors and the difference is reported). A debug entry point:
+ * the same call as mla_tree_verify, computed twice, by the tensor-core
+ * kernel into out / lse (what the caller gets) and by the warp-shuffle
+ * kernel into scratch inside the workspace; then, on the device,
+ *   diff[0] = max over elements |out_tc - out_simt|            (fp32 of bf16)
+ *   diff[1] = max over rows |lse_tc - lse_simt| / max(1, |lse_tc|)
+ *            (rows where both are -inf count 0; one -inf counts +inf)
+ * and MT_DEV_MISMATCH is set in dev_status when either exceeds tolerance.
+ *   diff: fp32 [2] device memory, overwritten by the call.
+ *   workspace: >= mla_tree_verify_validate_workspace_bytes(batch, total_q,
+ *            heads, max_splits) bytes, 256-byte aligned.
+ * Returns MT_EUNSUPPORTED when the tensor-core kernel cannot serve the call.
+ * The paper's gate compared against a separate reference backend; here the
+ * two paths are this library's own, written independently.
+ */
+size_t mla_tree_verify_validate_workspace_bytes(int batch, int total_q, int heads, int max_splits);
+int mla_tree_verify_validate(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                             const int32_t* kv_indices, int64_t kv_indices_len,
+                             const int32_t* kv_indptr, const int32_t* qo_indptr,
+                             const uint8_t* packed_mask, int64_t mask_len,
+                             const int64_t* mask_indptr, int batch, int total_q, int heads,
+                             float sm_scale, mt_bf16* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int max_splits, float tolerance,
+                             float* diff, int32_t* dev_status, mt_stream_t stream);
 
 /*
  * mla_tree_verify without a caller-provided workspace. The paper has no

@@ -14,12 +14,14 @@ LIB_PATH = os.path.join(_HERE, "lib", "libmla_tree.so")
 
 MT_OK, MT_EINVAL, MT_EUNSUPPORTED, MT_EWORKSPACE, MT_ECUDA = 0, -1, -2, -3, -4
 DEV_BAD_SLOT, DEV_BAD_PARENT, DEV_BAD_INDPTR, DEV_TREE_TOO_BIG, DEV_TIMEOUT = 1, 2, 4, 8, 16
+DEV_MISMATCH = 32
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 
 EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_scatter",
            "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits", "mla_tree_prepare",
            "mla_tree_verify_workspace_bytes", "mla_tree_verify_launch_count", "mla_tree_verify",
-           "mla_tree_verify_bits", "mla_tree_verify_noalloc"]
+           "mla_tree_verify_bits", "mla_tree_verify_validate_workspace_bytes",
+           "mla_tree_verify_validate", "mla_tree_verify_noalloc"]
 MT_ESCRATCH = -5
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -64,6 +66,11 @@ def load():
     lib.mla_tree_verify_bits.restype = I32
     lib.mla_tree_verify_bits.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                          P, P, P, SZ, I32, I32, P, P]
+    lib.mla_tree_verify_validate_workspace_bytes.restype = SZ
+    lib.mla_tree_verify_validate_workspace_bytes.argtypes = [I32, I32, I32, I32]
+    lib.mla_tree_verify_validate.restype = I32
+    lib.mla_tree_verify_validate.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
+                                             P, P, P, SZ, I32, F32, P, P, P]
     lib.mla_tree_verify_noalloc.restype = I32
     lib.mla_tree_verify_noalloc.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                             P, P, I32, I32, P, P]
@@ -217,6 +224,32 @@ def mla_tree_verify_bits(q, kv_buf, kv_indices, kv_indptr, qo_indptr, mask_words
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, path,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "mla_tree_verify_bits")
+
+
+def mla_tree_verify_validate_workspace_bytes(batch, total_q, heads, max_splits=0):
+    return int(load().mla_tree_verify_validate_workspace_bytes(batch, total_q, heads, max_splits))
+
+
+def mla_tree_verify_validate(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, mask_indptr,
+                             sm_scale, out, lse, workspace, diff, tolerance=1e-2, max_splits=0,
+                             status=None, stream=None):
+    """Validate mode: the call computed by both kernels; out/lse get the
+    tensor-core result, diff (fp32 [2] on the device) the max-abs output and
+    max relative LSE differences, status MT_DEV_MISMATCH beyond tolerance."""
+    if q.dim() != 3 or q.shape[2] != 576:
+        raise MlaTreeError("q must be [total_q, heads, 576]")
+    total_q, heads = q.shape[0], q.shape[1]
+    batch = qo_indptr.numel() - 1
+    rc = load().mla_tree_verify_validate(
+        _ptr(q, torch.bfloat16, "q"), _ptr(kv_buf, torch.bfloat16, "kv_buf"), kv_buf.shape[0],
+        _ptr(kv_indices, torch.int32, "kv_indices"), kv_indices.numel(),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(packed_mask, torch.uint8, "packed_mask"), packed_mask.numel(),
+        _ptr(mask_indptr, torch.int64, "mask_indptr"), batch, total_q, heads, float(sm_scale),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, float(tolerance),
+        _ptr(diff, torch.float32, "diff"), _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "mla_tree_verify_validate")
 
 
 def mla_tree_verify_noalloc(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, mask_indptr,

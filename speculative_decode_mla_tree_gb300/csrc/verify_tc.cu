@@ -70,7 +70,7 @@ constexpr int kMaxBatch = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
 constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
-constexpr int kSlotAhead = 4;    // key blocks whose slot numbers are in flight ahead of the gathers
+constexpr int kSlotAhead = 2;    // key blocks whose slot numbers are in flight ahead of the gathers
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kQRope = 0;                             // query rope half [128 rows x 64 B], 64B swizzle

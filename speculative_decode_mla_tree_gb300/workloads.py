@@ -147,15 +147,39 @@ def _draw_rows(count, g, latent_std=1.0, rope_std=1.0):
     return x.to(torch.bfloat16)
 
 
+def _draw_slots(total, num_slots, g, kv_layout):
+    """Distinct pool slots for ``total`` tokens.
+
+    shuffled:   a random permutation prefix of the pool (no two neighbours
+                adjacent in general);
+    contiguous: one run of consecutive slots at a random offset (a freshly
+                allocated or defragmented pool);
+    paged64:    random distinct pages of 64 consecutive slots, in random
+                order (a paged pool with 64-slot pages).
+    """
+    if kv_layout == "shuffled":
+        return torch.randperm(num_slots, generator=g)[:total].to(torch.int64)
+    if kv_layout == "contiguous":
+        off = int(torch.randint(0, num_slots - total + 1, (1,), generator=g))
+        return torch.arange(off, off + total, dtype=torch.int64)
+    if kv_layout == "paged64":
+        pages = (total + 63) // 64
+        pick = torch.randperm(num_slots // 64, generator=g)[:pages].to(torch.int64)
+        return (pick[:, None] * 64 + torch.arange(64)[None, :]).reshape(-1)[:total]
+    raise ValueError(kv_layout)
+
+
 def make_workload(name, heads, prefix_lens, tree_rules, tree_sizes, num_slots, seed,
-                  latent_std=1.0, rope_std=1.0, sm_scale=None, parents=None, g=None):
+                  latent_std=1.0, rope_std=1.0, sm_scale=None, parents=None, g=None,
+                  kv_layout="shuffled"):
     """Draw one workload.
 
     ``tree_rules`` is one rule name or a per-request list; ``parents`` may be
     given explicitly (list of per-request local parent lists) to build edge
-    cases. Slots for all prefix and draft tokens are distinct, drawn as one
-    random permutation prefix of the pool and handed out request by request:
-    the first P_b to the prefix, the next n_b to the draft tokens.
+    cases. Slots for all prefix and draft tokens are distinct, drawn by
+    ``kv_layout`` (see ``_draw_slots``; default a random permutation prefix
+    of the pool) and handed out request by request: the first P_b to the
+    prefix, the next n_b to the draft tokens.
     """
     if g is None:
         g = torch.Generator().manual_seed(seed)
@@ -170,7 +194,9 @@ def make_workload(name, heads, prefix_lens, tree_rules, tree_sizes, num_slots, s
     total_slots = sum(prefix_lens) + sum(tree_sizes)
     if total_slots > num_slots:
         raise ValueError("pool of %d slots cannot hold %d distinct rows" % (num_slots, total_slots))
-    slots = torch.randperm(num_slots, generator=g)[:total_slots].to(torch.int64)
+    if kv_layout == "paged64" and (total_slots + 63) // 64 > num_slots // 64:
+        raise ValueError("pool of %d slots cannot hold %d slots in 64-slot pages" % (num_slots, total_slots))
+    slots = _draw_slots(total_slots, num_slots, g, kv_layout)
 
     prefix_indices, out_cache_loc = [], []
     off = 0
@@ -198,7 +224,7 @@ def make_workload(name, heads, prefix_lens, tree_rules, tree_sizes, num_slots, s
         prefix_indices=torch.cat(prefix_indices).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         out_cache_loc=torch.cat(out_cache_loc).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         q=q, draft_kv=draft_kv, pool_slots=slots, pool_rows=pool_rows,
-        meta={"seed": seed, "rules": list(tree_rules) if tree_rules else None},
+        meta={"seed": seed, "rules": list(tree_rules) if tree_rules else None, "kv_layout": kv_layout},
     )
 
 
@@ -211,27 +237,29 @@ CONFIG_NAMES = {
 }
 
 
-def config(cid: int) -> Workload:
-    """The five benchmark configurations, seeded with 1000 + cid."""
+def config(cid: int, kv_layout: str = "shuffled") -> Workload:
+    """The five benchmark configurations, seeded with 1000 + cid. ``kv_layout``
+    varies only how pool slots are handed out (see ``_draw_slots``)."""
     g = torch.Generator().manual_seed(1000 + cid)
     seed = 1000 + cid
+    kw = {"g": g, "kv_layout": kv_layout}
     if cid == 1:
-        return make_workload("c1", 8, [21], "uniform", [9], 4096, seed, g=g)
+        return make_workload("c1", 8, [21], "uniform", [9], 4096, seed, **kw)
     if cid == 2:
         P = [int(torch.randint(1024, 4097, (1,), generator=g)) for _ in range(8)]
-        return make_workload("c2", 8, P, "branch3", [16] * 8, 65536, seed, g=g)
+        return make_workload("c2", 8, P, "branch3", [16] * 8, 65536, seed, **kw)
     if cid == 3:
         return make_workload("c3", 64, [8192] * 32, "branch4d8", [64] * 32, 300000, seed,
-                             latent_std=0.5, rope_std=1.0, g=g)
+                             latent_std=0.5, rope_std=1.0, **kw)
     if cid == 4:
-        return make_workload("c4", 16, [200000] * 4, "uniform", [32] * 4, 1 << 20, seed, g=g)
+        return make_workload("c4", 16, [200000] * 4, "uniform", [32] * 4, 1 << 20, seed, **kw)
     if cid == 5:
         lo, hi = math.log(128.0), math.log(131072.0)
         P = [int(math.floor(math.exp(lo + (hi - lo) * float(torch.rand((1,), generator=g)))))
              for _ in range(64)]
         n = [int(torch.randint(8, 65, (1,), generator=g)) for _ in range(64)]
         rules = ["chain" if b % 2 == 0 else "uniform" for b in range(64)]
-        return make_workload("c5", 64, P, rules, n, 1 << 22, seed, g=g)
+        return make_workload("c5", 64, P, rules, n, 1 << 22, seed, **kw)
     raise ValueError(cid)
 
 

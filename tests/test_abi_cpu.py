@@ -90,6 +90,17 @@ def test_host_argument_checks(lib):
     assert lib.mla_tree_prepare(*bad) == abi.MT_EINVAL
     bad = list(prep); bad[8] = 0
     assert lib.mla_tree_prepare(*bad) == abi.MT_OK
+    # validate mode: negative tolerance, missing diff, short workspace
+    val = list(args2[:18]) + [0, 1e-2, fake, null, null]
+    val[16] = fake; val[17] = 1 << 30
+    bad = list(val); bad[19] = -1.0
+    assert lib.mla_tree_verify_validate(*bad) == abi.MT_EINVAL
+    bad = list(val); bad[20] = null
+    assert lib.mla_tree_verify_validate(*bad) == abi.MT_EINVAL
+    bad = list(val); bad[17] = 256
+    assert lib.mla_tree_verify_validate(*bad) == abi.MT_EWORKSPACE
+    assert (lib.mla_tree_verify_validate_workspace_bytes(2, 32, 8, 4) >
+            lib.mla_tree_verify_workspace_bytes(2, 32, 8, 4) + 32 * 8 * 1024)
     # bit-form verify shares the verify checks
     args3 = list(args2); args3[16] = fake; args3[17] = 16
     assert lib.mla_tree_verify_bits(*args3) == abi.MT_EWORKSPACE

@@ -166,3 +166,38 @@ def test_prepare_flags_bad_slot_and_parent():
     st.prepare(); torch.cuda.synchronize()
     s = int(st.status.item())
     assert s & abi.DEV_BAD_SLOT and s & abi.DEV_BAD_PARENT
+
+
+@pytest.mark.parametrize("bits", [False, True], ids=["bytes", "bits"])
+@pytest.mark.parametrize("layout", ["contiguous", "paged64"])
+def test_kv_layouts_tc(layout, bits):
+    """Pools whose slots come in runs: one contiguous run, or 64-slot pages."""
+    w = W.config(2, layout)
+    st = VerifyStep(w, path=abi.PATH_TC, mask_bits=bits); st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    ref = OracleRun(w)
+    out, lse = ref.attention()
+    compare_attention(st.out, st.lse, out, lse)
+
+
+def test_contiguous_run_to_pool_end():
+    """A run ending at the last pool slot (the pool holds exactly the batch's
+    rows): the last block's rows past the split end read as zeros."""
+    w = W.make_workload("end", 8, [500, 300], "uniform", [16, 16], 832, seed=31, kv_layout="contiguous")
+    assert int(w.pool_slots.max()) == 831
+    for path in (abi.PATH_TC, abi.PATH_SIMT):
+        st = VerifyStep(w, path=path, fused=True); st.run(); torch.cuda.synchronize()
+        assert int(st.status.item()) == 0
+        ref = OracleRun(w)
+        out, lse = ref.attention()
+        compare_attention(st.out, st.lse, out, lse)
+
+
+def test_kv_layout_paged_long_prefix_sampled():
+    w = W.config(4, "paged64")
+    st = VerifyStep(w, path=abi.PATH_TC, fused=True); st.run(); torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    ref = OracleRun(w)
+    rows = sample_rows(w, 8, seed=44)
+    out, lse = ref.attention(rows=rows)
+    compare_attention(st.out, st.lse, out, lse, rows=rows)

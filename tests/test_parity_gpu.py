@@ -192,3 +192,28 @@ def test_empty_batch_is_noop():
                         torch.empty((0, 8, 512), dtype=torch.bfloat16, device="cuda"),
                         torch.empty((0, 8), dtype=torch.float32, device="cuda"),
                         torch.empty(256, dtype=torch.uint8, device="cuda"))
+
+
+def test_validate_mode_agrees_and_returns_tensor_core_result():
+    """Validate mode: out/lse equal a plain tensor-core call bit for bit, the
+    measured differences are within the verify tolerance, no mismatch bit;
+    with tolerance 0 the two kernels' rounding differences set it."""
+    w = W.config(2)
+    st = VerifyStep(w, path=abi.PATH_TC); st.run(); torch.cuda.synchronize()
+    nb = abi.mla_tree_verify_validate_workspace_bytes(w.batch, w.total_q, w.heads)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    diff = torch.full((2,), -1.0, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(st.out); lse = torch.empty_like(st.lse)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    abi.mla_tree_verify_validate(st.q, st.pool, st.kv_indices, st.kv_indptr, st.qo_indptr, st.mask,
+                                 st.mask_indptr, st.sm_scale, out, lse, ws, diff, 1e-2, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out, st.out) and torch.equal(lse, st.lse)
+    d = diff.cpu().tolist()
+    assert 0.0 <= d[0] <= 1e-2 and 0.0 <= d[1] <= 1e-3
+    abi.mla_tree_verify_validate(st.q, st.pool, st.kv_indices, st.kv_indptr, st.qo_indptr, st.mask,
+                                 st.mask_indptr, st.sm_scale, out, lse, ws, diff, 0.0, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & abi.DEV_MISMATCH
+    assert float(diff[0].item()) > 0.0

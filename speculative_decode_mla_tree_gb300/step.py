@@ -10,6 +10,25 @@ import torch
 from . import abi
 
 
+def _carve(dev, specs, buf=None):
+    """One uint8 buffer holding tensors of the given (shape, dtype), each at a
+    256-byte aligned offset; returns (buffer, views)."""
+    offs, off = [], 0
+    for shape, dtype in specs:
+        n = 1
+        for d in shape:
+            n *= int(d)
+        offs.append((off, n, shape, dtype))
+        off += -(-n * torch.empty((), dtype=dtype).element_size() // 256) * 256
+    if buf is None:
+        buf = torch.empty(max(off, 256), dtype=torch.uint8, device=dev)
+    views = []
+    for o, n, shape, dtype in offs:
+        es = torch.empty((), dtype=dtype).element_size()
+        views.append(buf[o:o + n * es].view(dtype).view(shape))
+    return buf, views
+
+
 class VerifyStep:
     def __init__(self, w, device="cuda", max_splits=0, path=abi.PATH_AUTO, pool=None,
                  mask_bits=False, fused=False):
@@ -29,14 +48,14 @@ class VerifyStep:
         L = [p + n for p, n in zip(w.prefix_lens, w.tree_sizes)]
         # resident latent-KV pool (before the draft rows are scattered in)
         self.pool = w.dense_pool(dev) if pool is None else pool
-        # per-step inputs
-        self.q = torch.empty_like(w.q, device=dev)
-        self.draft_kv = torch.empty_like(w.draft_kv, device=dev)
-        self.out_cache_loc = torch.empty_like(w.out_cache_loc, device=dev)
-        self.prefix_indices = torch.empty_like(w.prefix_indices, device=dev)
-        self.prefix_indptr = torch.empty_like(w.prefix_indptr, device=dev)
-        self.qo_indptr = torch.empty_like(w.qo_indptr, device=dev)
-        self.parents = torch.empty_like(w.parents, device=dev)
+        # per-step inputs: views into one device buffer, so that a step's
+        # inputs arrive with one host-to-device copy (see packed_inputs)
+        self._in_spec = [("q", w.q), ("draft_kv", w.draft_kv), ("out_cache_loc", w.out_cache_loc),
+                         ("prefix_indices", w.prefix_indices), ("prefix_indptr", w.prefix_indptr),
+                         ("qo_indptr", w.qo_indptr), ("parents", w.parents)]
+        self.inbuf, views = _carve(dev, [(h.shape, h.dtype) for _, h in self._in_spec])
+        for (name, _), v in zip(self._in_spec, views):
+            setattr(self, name, v)
         # intermediates and outputs
         self.kv_indices = torch.empty(sum(L), dtype=torch.int32, device=dev)
         self.kv_indptr = torch.empty(B + 1, dtype=torch.int32, device=dev)
@@ -46,8 +65,9 @@ class VerifyStep:
         self.mask_word_indptr = torch.empty(B + 1, dtype=torch.int64, device=dev)
         self.mask_words = torch.empty(sum(n * ((l + 31) // 32) for n, l in zip(w.tree_sizes, L)),
                                       dtype=torch.int32, device=dev)
-        self.out = torch.empty((T, w.heads, 512), dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty((T, w.heads), dtype=torch.float32, device=dev)
+        # outputs: views into one device buffer (one device-to-host copy)
+        self.outbuf, (self.out, self.lse) = _carve(dev, [((T, w.heads, 512), torch.bfloat16),
+                                                         ((T, w.heads), torch.float32)])
         nbytes = abi.mla_tree_verify_workspace_bytes(B, T, w.heads, max_splits)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -59,6 +79,15 @@ class VerifyStep:
         return [(self.q, w.q), (self.draft_kv, w.draft_kv), (self.out_cache_loc, w.out_cache_loc),
                 (self.prefix_indices, w.prefix_indices), (self.prefix_indptr, w.prefix_indptr),
                 (self.qo_indptr, w.qo_indptr), (self.parents, w.parents)]
+
+    def packed_inputs(self, pin=True):
+        """The per-step inputs packed in host memory with the layout of
+        ``inbuf``: ``inbuf.copy_(packed, non_blocking=True)`` loads a step."""
+        host = torch.zeros(self.inbuf.numel(), dtype=torch.uint8)
+        _, views = _carve(torch.device("cpu"), [(h.shape, h.dtype) for _, h in self._in_spec], host)
+        for v, (_, h) in zip(views, self._in_spec):
+            v.copy_(h)
+        return host.pin_memory() if pin else host
 
     def load(self, w=None):
         if w is not None:

@@ -71,6 +71,7 @@ constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
 constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
 constexpr int kSlotAhead = 2;    // key blocks whose slot numbers are in flight ahead of the gathers
+constexpr int kWarmBlocks = 512; // most key blocks per cluster (upper bound) for the dry-pass variant
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kQRope = 0;                             // query rope half [128 rows x 64 B], 64B swizzle
@@ -98,7 +99,8 @@ constexpr int B_O_DONE = B_P_FULL + 1;
 constexpr int B_O_FREE = B_O_DONE + 1;
 constexpr int B_DRAIN = B_O_FREE + 1;
 constexpr int kNumBars = B_DRAIN + 1;
-constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count
+constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count, B_DRY
+constexpr int B_DRY = (kMisc + 16 - kBars) / 8;       // never completes: the dry passes' waits and signals
 constexpr int kPlan = kMisc + 32;                     // per-request plan
 constexpr int kPlanStride = 9;                        // int32 words per request
 constexpr int kOrd = kPlan + kMaxBatch * kPlanStride * 4;   // request at each rank
@@ -106,6 +108,7 @@ constexpr int kOBase = kOrd + kMaxBatch * 4;          // first item of each rank
 constexpr int kSmemUsed = kOBase + (kMaxBatch + 1) * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kMisc % 8 == 0 && kBars + 8 * B_DRY + 8 <= kPlan, "B_DRY sits in the misc area");
 static_assert(2 * kXBytes >= BM * 128, "epilogue staging fits in one XO/XP pair");
 static_assert(BN % 16 == 0 && BN <= 64, "block width");
 static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
@@ -297,12 +300,15 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
 }
 
 // kBits: the tree mask is in the bit form (rows of ceil(L / 32) words)
-template <bool kBits>
+// kWarm: dry passes that load the softmax and sender loops' code before the
+// first scores arrive (worth it when each cluster has few blocks to do)
+template <bool kBits, bool kWarm>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ TcParams p,
                      const __grid_constant__ CUtensorMap tm_qrope,
                      const __grid_constant__ CUtensorMap tm_kvlat,
                      const __grid_constant__ CUtensorMap tm_kvrope) {
+  static_assert(kBits || !kWarm, "the softmax dry pass reads the bit-form mask");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -341,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_X_FREE0 + x], 8);    // own four softmax warps and the peer's, one arrival each
     }
     mbar_init(&bars[B_DRAIN], 1);
+    if (kWarm) mbar_init(&bars[B_DRY], (1 << 20) - 1);  // the largest count: its first phase never completes
     *abort = 0;
     fence_mbar_init_cluster();
   }
@@ -610,15 +617,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars[B_QT_FULL]);
       }
-      for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
+      // kWarm: the first item starts with a dry pass (blk = -1) as in the
+      // softmax warps: its waits and signals go to B_DRY, it reads O's
+      // columns (not written before the first P.V), writes only the own
+      // exchange buffer (rewritten before the softmax may read it) and
+      // sends nothing.
+      const int warm = (kWarm && rnd == 0) ? 1 : 0;
+      g -= warm;
+      for (int blk = -warm; blk < it.nblocks; ++blk, ++g) {
+        const bool dry = kWarm && blk < 0;
         const uint32_t b = g & 1;
-        mbar_wait<false>(&bars[B_S_FULL0 + b], (g >> 1) & 1, abort);
+        mbar_wait<false>(&bars[dry ? B_DRY : B_S_FULL0 + b], (g >> 1) & 1, abort);
         tc_fence_after();
         uint32_t s0[32], s1[16];
-        tmem_ld32(tmem + lane_base + kTmemS + 64 * b, s0);
-        tmem_ld16(tmem + lane_base + kTmemS + 64 * b + 32, s1);
+        const uint32_t tsrc = tmem + lane_base + (dry ? kTmemO : kTmemS + 64 * b);
+        tmem_ld32(tsrc, s0);
+        tmem_ld16(tsrc + 32, s1);
         tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
+        mbar_arrive(&bars[dry ? B_DRY : B_S_EMPTY0 + b]);  // the score buffer may take block g+2
         uint32_t h[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
@@ -633,18 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // both halves of buffer pair b are free: our softmax rows and the
         // peer's have read block g-2
-        mbar_wait<true>(&bars[B_X_FREE0 + b], ((g >> 1) & 1) ^ 1, abort);
+        mbar_wait<true>(&bars[dry ? B_DRY : B_X_FREE0 + b], (((g >> 1) & 1) ^ 1) | (dry ? 1u : 0u), abort);
         uint8_t* xo = sm + kX + 2 * b * kXBytes + r * kXRow;
         const uint32_t dst = xp_peer0 + 2 * b * kXBytes;
         const uint32_t bar = xfull_peer0 + 8 * b;
 #pragma unroll
         for (int q = 0; q < BN / 8; ++q) {
           *reinterpret_cast<uint4*>(xo + 16 * q) = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-          st_async_v4(dst + 16 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3], bar);
+          if (!dry) st_async_v4(dst + 16 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3], bar);
         }
         // own row written; r == 0 also arms the barrier for the peer's bytes
-        if (r == 0) mbar_arrive_expect_tx(&bars[B_X_FULL0 + b], (uint32_t)(BM * BN * 2));
-        else mbar_arrive(&bars[B_X_FULL0 + b]);
+        uint64_t* xfull = &bars[dry ? B_DRY : B_X_FULL0 + b];
+        if (r == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(BM * BN * 2));
+        else mbar_arrive(xfull);
       }
     }
   } else {
@@ -717,7 +734,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kBits) load_bits(0);
       else if (prefetch) load_mask(0);
       float m = -INFINITY, l = 0.f;
-      for (int blk = 0; blk < it.nblocks; ++blk, ++gblk) {
+      // kWarm: the first item starts with a dry pass (blk = -1) over the
+      // block body while the first scores are still in flight, only to pull
+      // the body's instructions into the SM's caches ahead of the real first
+      // block. It waits on and signals B_DRY (its wait parity, from a
+      // counter one below the first block's, is that of a phase counted as
+      // complete), releases nothing, and its P store lands in columns no
+      // MMA reads yet.
+      const int warm = (kWarm && rnd == 0) ? 1 : 0;
+      gblk -= warm;
+      for (int blk = -warm; blk < it.nblocks; ++blk, ++gblk) {
+        const bool dry = kWarm && blk < 0;
         const int jb = it.j0 + blk * BN;
         uint64_t vm;
         if (kBits) {
@@ -760,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // full scores (log2 domain): our fp16 partial plus the peer's
         const uint32_t xb = gblk & 1;
-        mbar_wait<true>(&bars[B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
+        mbar_wait<true>(&bars[dry ? B_DRY : B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
         const uint8_t* xo = sm + kX + 2 * xb * kXBytes + r * kXRow;
         const uint8_t* xp = xo + kXBytes;
         float s[BN];
@@ -778,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // the last block's pair stays ours: the epilogue stages rows in it
-        if (blk + 1 < it.nblocks) release_x(gblk);
+        if (kWarm ? (unsigned)blk < (unsigned)(it.nblocks - 1) : blk + 1 < it.nblocks) release_x(gblk);
 
         // masked online softmax (log2 domain)
         const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
@@ -846,7 +873,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL]);
+        mbar_arrive(&bars[dry ? B_DRY : B_P_FULL]);
+        if (dry) {
+          m = -INFINITY;
+          l = 0.f;
+        }
       }
       const uint32_t glast = gblk - 1;
 
@@ -992,10 +1023,12 @@ int device_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(g_dev_mu);
   if (g_clusters[dev] > 0) return g_clusters[dev];
-  if (cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(verify_tc_kernel<false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(verify_tc_kernel<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(verify_tc_kernel<true, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (num_sms / 2));
@@ -1009,7 +1042,7 @@ int device_clusters(int num_sms) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<false>, &cfg) != cudaSuccess || n <= 0)
+  if (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<false, false>, &cfg) != cudaSuccess || n <= 0)
     n = num_sms / 2;
   g_clusters[dev] = n;
   return n;
@@ -1050,9 +1083,16 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = a.bits_mask
-      ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, p, tq_rope, tkv_lat, tkv_rope)
-      : cudaLaunchKernelEx(&cfg, verify_tc_kernel<false>, p, tq_rope, tkv_lat, tkv_rope);
+  // The dry passes cost a few instructions in every block and save a few
+  // microseconds of instruction fetch once per CTA: they pay when each
+  // cluster has at most a few hundred key blocks to do. An upper bound from
+  // the host-known sizes (every tile against the whole kv_indices) decides.
+  const long long tiles_ub = ((long long)a.total_q * a.heads + BM - 1) / BM + a.batch;
+  const bool warm = a.bits_mask && tiles_ub * a.kv_len <= (long long)kWarmBlocks * BN * nclusters;
+  cudaError_t e =
+      !a.bits_mask ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<false, false>, p, tq_rope, tkv_lat, tkv_rope)
+      : warm       ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<true, true>, p, tq_rope, tkv_lat, tkv_rope)
+                   : cudaLaunchKernelEx(&cfg, verify_tc_kernel<true, false>, p, tq_rope, tkv_lat, tkv_rope);
   if (e != cudaSuccess) return e;
   if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
   return cudaSuccess;

@@ -58,17 +58,21 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def alg_cost(w, mask_bits=False):
+def alg_cost(w, mask_bits=False, skip_prefix=False):
     """Algorithmic bytes and flops of one verify call: every key row once,
     its index, the mask (a byte, or a bit in whole 32-bit words, per (row,
-    key)), q in, out and lse out; flops over visible (row, key) pairs only."""
+    key); with the prefix skip only the draft columns' bytes or words), q
+    in, out and lse out; flops over visible (row, key) pairs only."""
     H = w.heads
     qo = w.qo_indptr.tolist()
     byts, flops = 0, 0
     for b in range(w.batch):
         n, P = w.tree_sizes[b], w.prefix_lens[b]
         L = P + n
-        mask_bytes = n * 4 * ((L + 31) // 32) if mask_bits else n * L
+        if skip_prefix:  # draft columns only (the words that hold them)
+            mask_bytes = n * 4 * ((L + 31) // 32 - P // 32) if mask_bits else n * n
+        else:
+            mask_bytes = n * 4 * ((L + 31) // 32) if mask_bits else n * L
         byts += L * 1152 + L * 4 + mask_bytes + n * H * (1152 + 1024 + 4)
         par = w.parents[qo[b]:qo[b + 1]].tolist()
         depth = []
@@ -259,7 +263,7 @@ def run_ours(args):
     if fused and args.mask != "bits":
         raise SystemExit("--marshal fused packs the mask in its bit form: use --mask bits")
     st = VerifyStep(w, dev, max_splits=args.max_splits, path=args.path, mask_bits=args.mask == "bits",
-                    fused=fused)
+                    fused=fused, skip_prefix=args.skip_prefix)
     stream = torch.cuda.Stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
@@ -350,7 +354,7 @@ def run_ours(args):
 
     kv_bytes = w.kv_bytes()
     value = whole_job_gbs(world, args.steps, kv_bytes, total_ms)
-    byts, flops = alg_cost(w, args.mask == "bits")
+    byts, flops = alg_cost(w, args.mask == "bits", args.skip_prefix)
     verify_ms = statistics.mean(call_ms[-1])
     hbm, tf_burst, tf_sus, which = _peaks()
     achieved_gbs = byts / (verify_ms * 1e-3) / 1e9
@@ -403,6 +407,7 @@ def run_ours(args):
                        "draft_tokens": w.total_q, "kv_rows": kv_bytes // 1152,
                        "path": ["auto", "simt", "tensor-core"][args.path],
                        "max_splits": args.max_splits, "mask": args.mask, "marshal": args.marshal,
+                       "skip_prefix": args.skip_prefix,
                        "kv_layout": args.kv_layout,
                        "l2": "flushed between steps: 256 MiB written then read back, outside the events",
                        "timing": "whole step as one CUDA graph (value, ms_per_step); per-call graphs "
@@ -445,6 +450,8 @@ def main():
                     help="scatter, index marshaling and mask packing as one launch or three")
     ap.add_argument("--mask", default="bits", choices=["bytes", "bits"],
                     help="tree-mask form: one byte or one bit per (row, column)")
+    ap.add_argument("--skip-prefix", action="store_true",
+                    help="verify with the prefix-skip switch (prefix columns of the mask unread)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -251,6 +251,41 @@ int mla_tree_verify_bits(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
                          int32_t* dev_status, mt_stream_t stream);
 
 /*
+ * Mask options of mla_tree_verify_masked ("The Pivot to Live Cutover",
+ * section "The Technical Investigation: Probing the Integration Surface":
+ * the serving engine's attention kernel takes the tree mask with a switch
+ * that leaves the mask unread over the prefix columns).
+ *   MT_MASK_BITS         the mask is in the bit form of tree_mask_pack_bits
+ *                        (uint32 words; mask_len counts words), else bytes
+ *   MT_MASK_SKIP_PREFIX  columns j < P_b = L_b - n_b (the prefix) are
+ *                        visible to every draft row; their mask entries are
+ *                        never read and may hold anything. The layout of the
+ *                        mask (row stride L_b bytes or ceil(L_b / 32) words)
+ *                        is unchanged.
+ */
+#define MT_MASK_BITS 1
+#define MT_MASK_SKIP_PREFIX 2
+
+/*
+ * mla_tree_verify with the mask form and options as flags (a combination of
+ * MT_MASK_BITS and MT_MASK_SKIP_PREFIX; other bits give MT_EINVAL):
+ *     vis_j = 1                                   if SKIP_PREFIX and j < P_b
+ *           = the mask entry (i, j) of that form   otherwise
+ * mask: uint8 [mask_len] bytes, or uint32 [mask_len] words (4-byte aligned)
+ * with MT_MASK_BITS. flags 0 is mla_tree_verify, MT_MASK_BITS is
+ * mla_tree_verify_bits; everything else (arguments, outputs, workspace,
+ * paths, error behaviour) is theirs.
+ */
+int mla_tree_verify_masked(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                           const int32_t* kv_indices, int64_t kv_indices_len,
+                           const int32_t* kv_indptr, const int32_t* qo_indptr,
+                           const void* mask, int64_t mask_len, const int64_t* mask_indptr,
+                           int mask_flags, int batch, int total_q, int heads, float sm_scale,
+                           mt_bf16* out, float* lse,
+                           void* workspace, size_t workspace_bytes, int max_splits, int path,
+                           int32_t* dev_status, mt_stream_t stream);
+
+/*
  * Validate mode ("Deploying a Custom sm_120 Verify Kernel into Production",
  * "The Validate Mode": the custom kernel runs next to the reference path on
  * the same tensors and the difference is reported). A debug entry point:

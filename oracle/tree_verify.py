@@ -194,7 +194,7 @@ def _request_rows(qptr, heads, rows):
 
 
 def verify_attention(q_bits, kv_bits, kv_indices, kv_indptr, qo_indptr, packed_mask,
-                     mask_indptr, heads, sm_scale, rows=None, kv_range=None):
+                     mask_indptr, heads, sm_scale, rows=None, kv_range=None, skip_prefix=False):
     """Exact masked scaled-dot-product attention of every draft row.
 
     What the verify kernel computes ("Flipping the Switch" page, section "The
@@ -211,6 +211,10 @@ def verify_attention(q_bits, kv_bits, kv_indices, kv_indptr, qo_indptr, packed_m
     not overflow. ``rows`` restricts the work to a list of (t, h) pairs;
     ``kv_range`` = (lo, hi) restricts every request to logical positions
     [lo_b, hi_b) (a list of pairs, one per request) for split partials.
+    ``skip_prefix``: the switch that leaves the mask unread over the prefix
+    ("Pivot to Live Cutover" page, section "The Technical Investigation"):
+    the first P_b = L_b - n_b positions are visible to every row whatever
+    their mask bytes hold.
 
     Returns (out float64 [T, H, 512], lse float64 [T, H]); rows not computed
     are NaN.
@@ -233,7 +237,11 @@ def verify_attention(q_bits, kv_bits, kv_indices, kv_indptr, qo_indptr, packed_m
         slots = kidx[kptr[b] + lo:kptr[b] + hi]
         K = bf16_bits_to_f64(kvf_bits[slots, :D_QK])          # [Lr, 576]
         V = K[:, :D_V]                                        # [Lr, 512]
-        vis_all = mask[mptr[b]:mptr[b] + n * L].reshape(n, L)[:, lo:hi] != 0
+        vis_full = mask[mptr[b]:mptr[b] + n * L].reshape(n, L) != 0
+        if skip_prefix:
+            vis_full = vis_full.copy()
+            vis_full[:, :L - n] = True
+        vis_all = vis_full[:, lo:hi]
         ts = np.array([p[0] for p in pairs])
         hs = np.array([p[1] for p in pairs])
         Q = bf16_bits_to_f64(qf_bits[ts, hs, :D_QK])          # [R, 576]

@@ -20,7 +20,7 @@ PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_scatter",
            "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits", "mla_tree_prepare",
            "mla_tree_verify_workspace_bytes", "mla_tree_verify_launch_count", "mla_tree_verify",
-           "mla_tree_verify_bits", "mla_tree_verify_validate_workspace_bytes",
+           "mla_tree_verify_bits", "mla_tree_verify_masked", "mla_tree_verify_validate_workspace_bytes",
            "mla_tree_verify_validate", "mla_tree_verify_noalloc"]
 MT_ESCRATCH = -5
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -66,6 +66,9 @@ def load():
     lib.mla_tree_verify_bits.restype = I32
     lib.mla_tree_verify_bits.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                          P, P, P, SZ, I32, I32, P, P]
+    lib.mla_tree_verify_masked.restype = I32
+    lib.mla_tree_verify_masked.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, I32, F32,
+                                           P, P, P, SZ, I32, I32, P, P]
     lib.mla_tree_verify_validate_workspace_bytes.restype = SZ
     lib.mla_tree_verify_validate_workspace_bytes.argtypes = [I32, I32, I32, I32]
     lib.mla_tree_verify_validate.restype = I32
@@ -224,6 +227,32 @@ def mla_tree_verify_bits(q, kv_buf, kv_indices, kv_indptr, qo_indptr, mask_words
         _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), max_splits, path,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "mla_tree_verify_bits")
+
+
+MASK_BITS = 1         # the mask is in the bit form (int32 tensor of uint32 words)
+MASK_SKIP_PREFIX = 2  # prefix columns visible, their mask entries unread
+
+
+def mla_tree_verify_masked(q, kv_buf, kv_indices, kv_indptr, qo_indptr, mask, mask_indptr,
+                           mask_flags, sm_scale, out, lse, workspace, max_splits=0, path=PATH_AUTO,
+                           status=None, stream=None):
+    """mla_tree_verify with the mask form and options as flags (MASK_BITS,
+    MASK_SKIP_PREFIX): mask is a uint8 byte mask, or int32 words with
+    MASK_BITS."""
+    if q.dim() != 3 or q.shape[2] != 576:
+        raise MlaTreeError("q must be [total_q, heads, 576]")
+    total_q, heads = q.shape[0], q.shape[1]
+    batch = qo_indptr.numel() - 1
+    mdt = torch.int32 if mask_flags & MASK_BITS else torch.uint8
+    rc = load().mla_tree_verify_masked(
+        _ptr(q, torch.bfloat16, "q"), _ptr(kv_buf, torch.bfloat16, "kv_buf"), kv_buf.shape[0],
+        _ptr(kv_indices, torch.int32, "kv_indices"), kv_indices.numel(),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(qo_indptr, torch.int32, "qo_indptr"),
+        _ptr(mask, mdt, "mask"), mask.numel(), _ptr(mask_indptr, torch.int64, "mask_indptr"),
+        int(mask_flags), batch, total_q, heads, float(sm_scale), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        max_splits, path, _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "mla_tree_verify_masked")
 
 
 def mla_tree_verify_validate_workspace_bytes(batch, total_q, heads, max_splits=0):

@@ -184,9 +184,11 @@ int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_spli
 
 // One verify call with either mask form: bits = 0 uses packed_mask (bytes),
 // bits = 1 uses mask_words; mask_len counts the elements of that mask.
+// skip_prefix = 1: prefix columns are visible without reading the mask.
 static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
                          const int32_t* kv_indices, int64_t kv_indices_len,
                          const int32_t* kv_indptr, const int32_t* qo_indptr, int bits,
+                         int skip_prefix,
                          const uint8_t* packed_mask, const uint32_t* mask_words, int64_t mask_len,
                          const int64_t* mask_indptr, int batch, int total_q, int heads,
                          float sm_scale, mt_bf16* out, float* lse, void* workspace,
@@ -219,6 +221,7 @@ static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
   a.mask = bits ? nullptr : packed_mask;
   a.mask_bits = bits ? mask_words : nullptr;
   a.bits_mask = bits ? 1 : 0;
+  a.skip_prefix = skip_prefix ? 1 : 0;
   a.mask_len = mask_len;
   a.mask_indptr = mask_indptr;
   a.batch = batch;
@@ -265,7 +268,7 @@ int mla_tree_verify(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
                     const int64_t* mask_indptr, int batch, int total_q, int heads, float sm_scale,
                     mt_bf16* out, float* lse, void* workspace, size_t workspace_bytes,
                     int max_splits, int path, int32_t* dev_status, mt_stream_t stream) {
-  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 0,
+  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 0, 0,
                        packed_mask, nullptr, mask_len, mask_indptr, batch, total_q, heads,
                        sm_scale, out, lse, workspace, workspace_bytes, max_splits, path,
                        dev_status, stream);
@@ -279,9 +282,26 @@ int mla_tree_verify_bits(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
                          float sm_scale, mt_bf16* out, float* lse, void* workspace,
                          size_t workspace_bytes, int max_splits, int path, int32_t* dev_status,
                          mt_stream_t stream) {
-  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 1,
+  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, 1, 0,
                        nullptr, mask_words, mask_len_words,
                        mask_word_indptr, batch, total_q, heads, sm_scale, out, lse, workspace,
+                       workspace_bytes, max_splits, path, dev_status, stream);
+}
+
+int mla_tree_verify_masked(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,
+                           const int32_t* kv_indices, int64_t kv_indices_len,
+                           const int32_t* kv_indptr, const int32_t* qo_indptr, const void* mask,
+                           int64_t mask_len, const int64_t* mask_indptr, int mask_flags,
+                           int batch, int total_q, int heads, float sm_scale, mt_bf16* out,
+                           float* lse, void* workspace, size_t workspace_bytes, int max_splits,
+                           int path, int32_t* dev_status, mt_stream_t stream) {
+  if (mask_flags & ~(MT_MASK_BITS | MT_MASK_SKIP_PREFIX)) return MT_EINVAL;
+  const int bits = (mask_flags & MT_MASK_BITS) ? 1 : 0;
+  if (bits && (uintptr_t)mask % 4) return MT_EINVAL;
+  return verify_common(q, kv_buf, num_slots, kv_indices, kv_indices_len, kv_indptr, qo_indptr, bits,
+                       (mask_flags & MT_MASK_SKIP_PREFIX) ? 1 : 0,
+                       bits ? nullptr : (const uint8_t*)mask, bits ? (const uint32_t*)mask : nullptr,
+                       mask_len, mask_indptr, batch, total_q, heads, sm_scale, out, lse, workspace,
                        workspace_bytes, max_splits, path, dev_status, stream);
 }
 

@@ -18,6 +18,8 @@ struct VerifyArgs {
   const uint8_t* mask;           // byte mask, or nullptr when mask_bits is set
   const uint32_t* mask_bits;     // bit-form mask (rows of ceil(L / 32) words)
   int bits_mask;                 // 1: the mask is mask_bits, 0: it is mask (bytes)
+  int skip_prefix;               // 1: prefix columns (j < L - n) are visible and their
+                                 //   mask entries are not read
   int64_t mask_len;              // elements of that mask
   const int64_t* mask_indptr;
   int batch, total_q, heads;

@@ -101,14 +101,16 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   // this token's mask row: L bytes, or ceil(L / 32) words of the bit form
   const int64_t mrow0 = g.mask0 + (t - g.q0) * (int64_t)g.mask_row;
   const int32_t* idx = a.kv_indices + g.kv0;
+  const int pre = a.skip_prefix ? g.L - g.n : 0;  // columns visible without a mask read
   for (int j = j0; j < j1; ++j) {
     const int32_t slot = __ldg(idx + j);
     if (slot < 0 || slot >= a.num_slots) {
       if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
       continue;
     }
-    const bool vis = a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u)
-                                  : __ldg(a.mask + mrow0 + j) != 0;
+    const bool vis = j < pre ? true
+                     : a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u)
+                                   : __ldg(a.mask + mrow0 + j) != 0;
     if (!vis) continue;
     float kf[18];
     load_row18(a.kv + (int64_t)slot * kDqk, lane, 1.f, kf);

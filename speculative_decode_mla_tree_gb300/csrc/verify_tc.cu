@@ -302,7 +302,8 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
 // kBits: the tree mask is in the bit form (rows of ceil(L / 32) words)
 // kWarm: dry passes that load the softmax and sender loops' code before the
 // first scores arrive (worth it when each cluster has few blocks to do)
-template <bool kBits, bool kWarm>
+// kSkip: prefix columns are visible and their mask entries are not read
+template <bool kBits, bool kWarm, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ TcParams p,
                      const __grid_constant__ CUtensorMap tm_qrope,
@@ -704,6 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // thread r owns pairs r + 128 k. When a tile touches few enough nodes
       // (every case with 8 or more heads), the bytes of block blk+1 are
       // loaded while block blk is processed.
+      const int pre = kSkip ? it.L - it.n : 0;  // prefix columns: visible, mask unread
       constexpr int kGroups = BN / 8;  // 8-column groups per block row
       const int pairs = cnt * kGroups;
       const bool prefetch = pairs <= 128 * kMaskPrefetch;
@@ -717,7 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos0 = jb_ + 8 * (q % kGroups);
             const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) raw[k][e] = pos0 + e < it.j1 ? __ldg(src + e) : 0;
+            for (int e = 0; e < 8; ++e)
+              raw[k][e] = pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) ? __ldg(src + e) : 0;
           }
         }
       };
@@ -729,7 +732,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_bits = [&](int blk_) {
         const int wi = (it.j0 + blk_ * BN) >> 5;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) mnext[k] = wi + k < mw ? __ldg(mrow + wi + k) : 0u;
+        for (int k = 0; k < 3; ++k)
+          mnext[k] = wi + k < mw && (!kSkip || 32 * (wi + k) + 32 > pre) ? __ldg(mrow + wi + k) : 0u;
       };
       if (kBits) load_bits(0);
       else if (prefetch) load_mask(0);
@@ -777,12 +781,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bits = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              if (pos0 + e < it.j1 && __ldg(src + e)) bits |= 1u << e;
+              if (pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) && __ldg(src + e)) bits |= 1u << e;
             vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
           }
         }
         named_bar_sync(1, 128);
         vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
+        }
+        if (kSkip && pre > jb) {  // the block's prefix columns, up to the split's end
+          const int pc = min(pre, it.j1) - jb;
+          vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
         }
 
         // full scores (log2 domain): our fp16 partial plus the peer's
@@ -1017,19 +1025,35 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+using KernelFn = void (*)(TcParams, CUtensorMap, CUtensorMap, CUtensorMap);
+
+// The instantiations: byte mask (no dry pass) or bit mask, each with and
+// without the prefix skip.
+constexpr int kVariants = 6;
+KernelFn kernel_variant(int i) {
+  switch (i) {
+    case 0: return verify_tc_kernel<false, false, false>;
+    case 1: return verify_tc_kernel<false, false, true>;
+    case 2: return verify_tc_kernel<true, false, false>;
+    case 3: return verify_tc_kernel<true, false, true>;
+    case 4: return verify_tc_kernel<true, true, false>;
+    default: return verify_tc_kernel<true, true, true>;
+  }
+}
+int variant_index(bool bits, bool warm, bool skip) {
+  return !bits ? (skip ? 1 : 0) : (warm ? 4 : 2) + (skip ? 1 : 0);
+}
+
 // Clusters of two that fit at once on this device (persistent grid size).
 int device_clusters(int num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(g_dev_mu);
   if (g_clusters[dev] > 0) return g_clusters[dev];
-  if (cudaFuncSetAttribute(verify_tc_kernel<false, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(verify_tc_kernel<true, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(verify_tc_kernel<true, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-    return 0;
+  for (int i = 0; i < kVariants; ++i)
+    if (cudaFuncSetAttribute(kernel_variant(i), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (num_sms / 2));
   cfg.blockDim = dim3(kThreads);
@@ -1042,7 +1066,7 @@ int device_clusters(int num_sms) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<false, false>, &cfg) != cudaSuccess || n <= 0)
+  if (cudaOccupancyMaxActiveClusters(&n, kernel_variant(0), &cfg) != cudaSuccess || n <= 0)
     n = num_sms / 2;
   g_clusters[dev] = n;
   return n;
@@ -1089,10 +1113,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   // the host-known sizes (every tile against the whole kv_indices) decides.
   const long long tiles_ub = ((long long)a.total_q * a.heads + BM - 1) / BM + a.batch;
   const bool warm = a.bits_mask && tiles_ub * a.kv_len <= (long long)kWarmBlocks * BN * nclusters;
-  cudaError_t e =
-      !a.bits_mask ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<false, false>, p, tq_rope, tkv_lat, tkv_rope)
-      : warm       ? cudaLaunchKernelEx(&cfg, verify_tc_kernel<true, true>, p, tq_rope, tkv_lat, tkv_rope)
-                   : cudaLaunchKernelEx(&cfg, verify_tc_kernel<true, false>, p, tq_rope, tkv_lat, tkv_rope);
+  const KernelFn fn = kernel_variant(variant_index(a.bits_mask != 0, warm, a.skip_prefix != 0));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p, tq_rope, tkv_lat, tkv_rope);
   if (e != cudaSuccess) return e;
   if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
   return cudaSuccess;

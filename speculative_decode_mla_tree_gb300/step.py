@@ -31,10 +31,12 @@ def _carve(dev, specs, buf=None):
 
 class VerifyStep:
     def __init__(self, w, device="cuda", max_splits=0, path=abi.PATH_AUTO, pool=None,
-                 mask_bits=False, fused=False):
+                 mask_bits=False, fused=False, skip_prefix=False):
         """mask_bits: pack the tree mask in its bit form; fused (implies
         mask_bits): scatter, index marshaling and mask packing as one launch
-        (mla_tree_prepare)."""
+        (mla_tree_prepare); skip_prefix: verify with the prefix-skip switch
+        (the prefix columns of the mask are not read)."""
+        self.skip_prefix = bool(skip_prefix)
         dev = torch.device(device)
         self.device = dev
         self.w = w
@@ -120,6 +122,15 @@ class VerifyStep:
                                self.mask, self.status, stream)
 
     def verify(self, stream=None):
+        if self.skip_prefix:
+            flags = abi.MASK_SKIP_PREFIX | (abi.MASK_BITS if self.mask_bits else 0)
+            mask, mptr = ((self.mask_words, self.mask_word_indptr) if self.mask_bits
+                          else (self.mask, self.mask_indptr))
+            abi.mla_tree_verify_masked(self.q, self.pool, self.kv_indices, self.kv_indptr,
+                                       self.qo_indptr, mask, mptr, flags, self.sm_scale, self.out,
+                                       self.lse, self.workspace, self.max_splits, self.path,
+                                       self.status, stream)
+            return
         if self.mask_bits:
             abi.mla_tree_verify_bits(self.q, self.pool, self.kv_indices, self.kv_indptr, self.qo_indptr,
                                      self.mask_words, self.mask_word_indptr, self.sm_scale, self.out,

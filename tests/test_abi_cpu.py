@@ -106,6 +106,15 @@ def test_host_argument_checks(lib):
     assert lib.mla_tree_verify_bits(*args3) == abi.MT_EWORKSPACE
     args3[12] = 0
     assert lib.mla_tree_verify_bits(*args3) == abi.MT_EINVAL
+    # the flags form: unknown flag bits, a misaligned word mask, then the
+    # shared checks
+    args4 = list(args2[:10]) + [abi.MASK_SKIP_PREFIX] + list(args2[10:])
+    args4[17] = fake; args4[18] = 16
+    assert lib.mla_tree_verify_masked(*args4) == abi.MT_EWORKSPACE
+    bad = list(args4); bad[10] = 4
+    assert lib.mla_tree_verify_masked(*bad) == abi.MT_EINVAL
+    bad = list(args4); bad[10] = abi.MASK_BITS | abi.MASK_SKIP_PREFIX; bad[7] = fake + 2
+    assert lib.mla_tree_verify_masked(*bad) == abi.MT_EINVAL
 
 
 def test_workspace_size_grows_with_splits(lib):

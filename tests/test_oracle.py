@@ -222,6 +222,42 @@ def test_chain_is_causal_decode():
             assert np.abs(np.array(o) - out[i, h]).max() < 1e-11
 
 
+def test_skip_prefix_reads_no_prefix_mask():
+    """The prefix-skip switch: the first L_b - n_b positions are visible
+    whatever their mask bytes hold, the draft positions still follow the tree."""
+    w = W.make_workload("skip", 2, [6, 9], "uniform", [5, 7], 128, seed=21)
+    pool, kv_indices, kv_indptr, mask_indptr, mask = _prepare(w)
+    out, lse = _attend(w, pool, kv_indices, kv_indptr, mask_indptr, mask)
+    # a tree mask already shows the whole prefix: the switch changes nothing
+    o2, l2 = _attend(w, pool, kv_indices, kv_indptr, mask_indptr, mask, skip_prefix=True)
+    assert np.array_equal(o2, out) and np.array_equal(l2, lse)
+    # clear every prefix byte
+    cleared = mask.copy()
+    qptr = w.qo_indptr.numpy()
+    for b in range(len(qptr) - 1):
+        n, L = int(qptr[b + 1] - qptr[b]), int(kv_indptr[b + 1] - kv_indptr[b])
+        for i in range(n):
+            cleared[mask_indptr[b] + i * L:mask_indptr[b] + i * L + L - n] = 0
+    o3, l3 = _attend(w, pool, kv_indices, kv_indptr, mask_indptr, cleared, skip_prefix=True)
+    assert np.array_equal(o3, out) and np.array_equal(l3, lse)
+    # without the switch the cleared prefix is gone: a root (parent -1) sees
+    # only itself, so its row is that key's value row and its own score
+    o4, l4 = _attend(w, pool, kv_indices, kv_indptr, mask_indptr, cleared)
+    scale = float(np.float32(w.sm_scale))
+    for b in range(len(qptr) - 1):
+        n, L = int(qptr[b + 1] - qptr[b]), int(kv_indptr[b + 1] - kv_indptr[b])
+        for i in range(n):
+            if int(w.parents[qptr[b] + i]) != -1:
+                continue
+            t = int(qptr[b]) + i
+            k = oracle.bf16_bits_to_f64(pool[int(kv_indices[kv_indptr[b] + L - n + i])])
+            for h in range(w.heads):
+                qf = oracle.bf16_bits_to_f64(_bits(w.q)[t, h])
+                assert abs(l4[t, h] - scale * float(qf @ k)) < 1e-9
+                assert np.abs(o4[t, h] - k[:512]).max() < 1e-12
+    assert not np.allclose(o4, out)
+
+
 def test_constant_scores_give_uniform_mean():
     """Zero latent query dims and one shared rope key make every score equal:
     out is the plain mean of the visible V rows, lse = s + ln(#visible)."""

@@ -185,30 +185,47 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
 
 // ---------------------------------------------------------------- merge
 
-// One CTA per (token, group of kMergeHeads heads); thread (h, d) owns output
-// dims [4 d, 4 d + 4) of head h of the group:
-//   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
-// The producing kernel records each token's split count, so one load decides
-// the work; then every split's LSE and partial are loaded at once (up to
-// kMergeRegSplits splits): two dependent memory rounds per row. Tokens of
-// unsplit requests were finished in place.
-// Partials are fp32 (warp-shuffle path) or fp16 (tensor-core path).
-constexpr int kMergeHeads = 1;
-constexpr int kMergeThreads = kMergeHeads * (kDv / 4);
-constexpr int kMergeRegSplits = 12;
+// lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
+// One CTA per (token, group of heads). Each thread owns the 16 bytes of a
+// partial row that one vector load brings in: 8 dims of an fp16 partial
+// (tensor-core path) or 4 of an fp32 one (warp-shuffle path). The producing
+// kernel records each token's split count, so one load decides the work.
+// Then the LSEs and partials of up to kMergeGroup splits are loaded at once:
+// two dependent memory rounds per row. More splits are taken in further
+// groups of the same size, with the running maximum rescaled between
+// groups. Tokens of unsplit requests were finished in place.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeGroup = 12;
 
-__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ float4 load4(const __half* p) {
-  const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
-  const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
-  return make_float4(lo.x, lo.y, hi.x, hi.y);
+template <typename P>
+struct MergeShape {
+  static constexpr int kVec = 16 / (int)sizeof(P);              // dims per thread
+  static constexpr int kThreadsPerHead = kDv / kVec;
+  static constexpr int kHeads = kMergeThreads / kThreadsPerHead;  // heads per CTA
+};
+
+__device__ __forceinline__ void unpack16(const uint4 u, const float*, float (&x)[4]) {
+  x[0] = __uint_as_float(u.x);
+  x[1] = __uint_as_float(u.y);
+  x[2] = __uint_as_float(u.z);
+  x[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4 u, const __half*, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+  }
 }
 
 template <typename P>
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyArgs a) {
+  using Shape = MergeShape<P>;
+  constexpr int kVec = Shape::kVec;
   const int tid = threadIdx.x;
-  const int hl = tid / (kDv / 4), d4 = tid % (kDv / 4);
+  const int hl = tid / Shape::kThreadsPerHead, dv = tid % Shape::kThreadsPerHead;
   const int64_t t = blockIdx.x;
   // When launched as a dependent grid of the producing kernel, wait for it
   // to complete (and its writes to be visible) before reading anything it
@@ -216,60 +233,66 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // split count of the token's request, recorded by the producing kernel
   // (0 or 1: nothing to merge)
-  const int S = __ldcg(a.ws_tok + t);
-  if (S <= 1 || S > a.max_splits) return;
-  const int h = blockIdx.y * kMergeHeads + hl;
-  if (S == 0 || h >= a.heads) return;
+  const int ns = __ldcg(a.ws_tok + t);
+  if (ns <= 1 || ns > a.max_splits) return;
+  const int h = blockIdx.y * Shape::kHeads + hl;
+  if (h >= a.heads) return;
   const int64_t R = (int64_t)a.total_q * a.heads;
   const int64_t row = t * a.heads + h;
-  const P* base = reinterpret_cast<const P*>(a.ws_o) + row * kDv + 4 * d4;
+  const P* base = reinterpret_cast<const P*>(a.ws_o) + row * kDv + kVec * dv;
   const int64_t step = R * kDv;  // elements between two splits of one row
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[kVec];
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
   float tot = 0.f, mx = -INFINITY;
-  if (S <= kMergeRegSplits) {
-    float ls[kMergeRegSplits];
-    float4 v[kMergeRegSplits];
+#pragma unroll 1
+  for (int g0 = 0; g0 < ns; g0 += kMergeGroup) {
+    float ls[kMergeGroup];
+    uint4 v[kMergeGroup];
+    const float* pl = a.ws_lse + (int64_t)g0 * R + row;
+    const P* po = base + (int64_t)g0 * step;
 #pragma unroll
-    for (int s = 0; s < kMergeRegSplits; ++s)
-      if (s < S) {
-        ls[s] = __ldg(a.ws_lse + (int64_t)s * R + row);
-        v[s] = load4(base + (int64_t)s * step);
+    for (int s = 0; s < kMergeGroup; ++s, pl += R, po += step)
+      if (g0 + s < ns) {
+        ls[s] = __ldg(pl);
+        v[s] = __ldg(reinterpret_cast<const uint4*>(po));
       }
+    float gm = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMergeRegSplits; ++s)
-      if (s < S) mx = fmaxf(mx, ls[s]);
+    for (int s = 0; s < kMergeGroup; ++s)
+      if (g0 + s < ns) gm = fmaxf(gm, ls[s]);
+    if (gm == -INFINITY) continue;  // every split of this group saw nothing
+    if (gm > mx) {  // rescale what earlier groups summed (nothing on the first)
+      const float c = exp2f((mx - gm) * kLog2e);
+      tot *= c;
 #pragma unroll
-    for (int s = 0; s < kMergeRegSplits; ++s)
-      if (s < S && mx != -INFINITY && ls[s] != -INFINITY) {
-        const float w = exp2f((ls[s] - mx) * kLog2e);
-        tot += w;
-        acc.x = fmaf(w, v[s].x, acc.x);
-        acc.y = fmaf(w, v[s].y, acc.y);
-        acc.z = fmaf(w, v[s].z, acc.z);
-        acc.w = fmaf(w, v[s].w, acc.w);
-      }
-  } else {
-    for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(a.ws_lse + (int64_t)s * R + row));
-    for (int s = 0; s < S && mx != -INFINITY; ++s) {
-      const float l2 = __ldg(a.ws_lse + (int64_t)s * R + row);
-      if (l2 == -INFINITY) continue;
-      const float w = exp2f((l2 - mx) * kLog2e);
-      const float4 x = load4(base + (int64_t)s * step);
-      tot += w;
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+      for (int e = 0; e < kVec; ++e) acc[e] *= c;
+      mx = gm;
     }
+#pragma unroll
+    for (int s = 0; s < kMergeGroup; ++s)
+      if (g0 + s < ns && ls[s] != -INFINITY) {
+        const float w = exp2f((ls[s] - mx) * kLog2e);
+        float x[kVec];
+        unpack16(v[s], static_cast<const P*>(nullptr), x);
+        tot += w;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+      }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 w2;
-  w2.x = *reinterpret_cast<const uint32_t*>(&lo);
-  w2.y = *reinterpret_cast<const uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(a.out + row * kDv)[d4] = w2;
-  if (d4 == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  uint32_t o[kVec / 2];
+#pragma unroll
+  for (int e = 0; e < kVec / 2; ++e) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    o[e] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint16_t* dst = a.out + row * kDv + kVec * dv;
+  if (kVec == 8)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2 % (kVec / 2)], o[3 % (kVec / 2)]);  // kVec / 2 == 4 here
+  else
+    *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+  if (dv == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
@@ -277,7 +300,8 @@ cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
   // producing kernel drains and waits on-device for its completion, which
   // hides the launch gap between the two.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.total_q, (unsigned)((a.heads + kMergeHeads - 1) / kMergeHeads));
+  const int heads_per_cta = a.partial_f16 ? MergeShape<__half>::kHeads : MergeShape<float>::kHeads;
+  cfg.gridDim = dim3((unsigned)a.total_q, (unsigned)((a.heads + heads_per_cta - 1) / heads_per_cta));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr;

@@ -135,8 +135,81 @@ cudaError_t launch_kv_indices_build(const int32_t* pidx, int64_t pidx_len, const
 
 // ---------------------------------------------------------------- tree mask
 
+// Block-wide sum of v; every thread gets it. red: shared scratch of 32.
+__device__ __forceinline__ long long block_sum(long long v, long long* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();  // red may still be read after a previous call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+  return t;
+}
+
+// Block-wide inclusive scan of v in thread order; *total gets the sum.
+__device__ __forceinline__ long long block_scan(long long v, long long* red, long long* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  __syncthreads();
+  if (lane == 31) red[w] = v;
+  __syncthreads();
+  long long before = 0, tot = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+    if (i < w) before += red[i];
+    tot += red[i];
+  }
+  *total = tot;
+  return v + before;
+}
+
+// Where request b's mask starts: the sum over requests r < b of n_r * row_r
+// (row_r: its row length in mask elements, from row_len(r)), with the
+// requests loaded by all the block's threads at once; bad counts earlier
+// requests with n < 0 or L < n. With write_indptr the block also writes the
+// offsets of every request (indptr[r + 1] = sum over r' <= r of the valid
+// n * row terms), as a block-wide scan.
+template <typename RowLen>
+__device__ __forceinline__ void mask_offsets(const int32_t* __restrict__ qptr, int batch, int b,
+                                             RowLen row_len, bool write_indptr, int64_t* indptr,
+                                             long long* base, long long* bad) {
+  __shared__ long long red[32];
+  long long part = 0, nbad = 0;
+  for (int r = threadIdx.x; r < b; r += blockDim.x) {
+    const long long n = (long long)qptr[r + 1] - qptr[r];
+    long long L;
+    const long long row = row_len(r, &L);
+    if (n < 0 || L < n) ++nbad;
+    part += n * row;
+  }
+  *base = block_sum(part, red);
+  *bad = block_sum(nbad, red);
+  if (!write_indptr) return;
+  if (threadIdx.x == 0) indptr[0] = 0;
+  long long carry = 0;
+  for (int c0 = 0; c0 < batch; c0 += blockDim.x) {
+    const int r = c0 + threadIdx.x;
+    long long term = 0;
+    if (r < batch) {
+      const long long n = (long long)qptr[r + 1] - qptr[r];
+      long long L;
+      const long long row = row_len(r, &L);
+      term = (n >= 0 && L >= n) ? n * row : 0;
+    }
+    long long tot;
+    const long long incl = block_scan(term, red, &tot);
+    if (r < batch) indptr[r + 1] = carry + incl;
+    carry += tot;
+  }
+}
+
 // grid (row groups, batch). Each CTA: compute its request's mask offset by
-// summing n*L over earlier requests; for each of its rows, walk the parent
+// summing n*L over earlier requests (all threads loading at once); for each
+// of its rows, walk the parent
 // chain once into a shared bitset, then write the row: prefix bytes 1, draft
 // byte k = bit k. Interior 16-byte chunks go out as one vector store; the
 // head and tail bytes of a row (which may share a 16-byte chunk with the
@@ -154,33 +227,15 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
     const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ mask_indptr,
     uint8_t* __restrict__ mask, int64_t capacity, int32_t* status) {
   __shared__ uint32_t bits[MT_MAX_TREE / 32];
-  __shared__ long long s_base;
-  __shared__ int s_bad;
   const int b = blockIdx.y;
-  if (threadIdx.x == 0) {
-    long long base = 0;
-    int bad = 0;
-    for (int r = 0; r < b; ++r) {
-      const long long n = (long long)qptr[r + 1] - qptr[r];
-      const long long L = (long long)kptr[r + 1] - kptr[r];
-      if (n < 0 || L < n) bad = 1;
-      base += n * L;
-    }
-    s_base = base;
-    s_bad = bad;
-    if (b == 0 && blockIdx.x == 0) {
-      // Offsets for every request (serial: batch is small).
-      long long acc = 0;
-      mask_indptr[0] = 0;
-      for (int r = 0; r < batch; ++r) {
-        const long long n = (long long)qptr[r + 1] - qptr[r];
-        const long long L = (long long)kptr[r + 1] - kptr[r];
-        acc += (n >= 0 && L >= n) ? n * L : 0;
-        mask_indptr[r + 1] = acc;
-      }
-    }
-  }
-  __syncthreads();
+  long long s_base, s_bad;
+  mask_offsets(
+      qptr, batch, b,
+      [&](int r, long long* L) {
+        *L = (long long)kptr[r + 1] - kptr[r];
+        return *L;
+      },
+      b == 0 && blockIdx.x == 0, mask_indptr, &s_base, &s_bad);
   const int64_t q0 = qptr[b];
   const int64_t n = (int64_t)qptr[b + 1] - q0;
   const int64_t L = (int64_t)kptr[b + 1] - kptr[b];
@@ -291,31 +346,14 @@ __device__ __forceinline__ void mask_bits_body(
     int64_t* __restrict__ word_indptr, uint32_t* __restrict__ words, int64_t capacity,
     int32_t* status, int b, int g, int groups) {
   __shared__ uint32_t bits[MT_MAX_TREE / 32];
-  __shared__ long long s_base;
-  __shared__ int s_bad;
-  if (threadIdx.x == 0) {
-    long long base = 0;
-    int bad = 0;
-    for (int r = 0; r < b; ++r) {
-      const long long n = (long long)qptr[r + 1] - qptr[r];
-      const long long L = req_len(kptr, pptr, qptr, r);
-      if (n < 0 || L < n) bad = 1;
-      base += n * ((L + 31) >> 5);
-    }
-    s_base = base;
-    s_bad = bad;
-    if (b == 0 && g == 0) {
-      long long acc = 0;
-      word_indptr[0] = 0;
-      for (int r = 0; r < batch; ++r) {
-        const long long n = (long long)qptr[r + 1] - qptr[r];
-        const long long L = req_len(kptr, pptr, qptr, r);
-        acc += (n >= 0 && L >= n) ? n * ((L + 31) >> 5) : 0;
-        word_indptr[r + 1] = acc;
-      }
-    }
-  }
-  __syncthreads();
+  long long s_base, s_bad;
+  mask_offsets(
+      qptr, batch, b,
+      [&](int r, long long* L) {
+        *L = req_len(kptr, pptr, qptr, r);
+        return (*L + 31) >> 5;
+      },
+      b == 0 && g == 0, word_indptr, &s_base, &s_bad);
   const int64_t q0 = qptr[b];
   const int64_t n = (int64_t)qptr[b + 1] - q0;
   const int64_t L = req_len(kptr, pptr, qptr, b);

@@ -45,10 +45,6 @@ WorkspaceLayout workspace_layout(int batch, int total_q, int heads, int max_spli
   off = align_up(off + sizeof(float) * (size_t)max_splits * rows, 256);
   w.o_off = off;
   off = align_up(off + sizeof(float) * (size_t)max_splits * rows * MT_D_V, 256);
-  w.counter_off = off;
-  // one arrival counter per 128-row tile (tiles never straddle requests)
-  w.counter_len = (int64_t)((rows + 127) / 128 + (size_t)batch + 1);
-  off = align_up(off + sizeof(int32_t) * (size_t)w.counter_len, 256);
   w.total = off;
   return w;
 }
@@ -237,8 +233,6 @@ static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
   a.ws_tok = (int32_t*)(ws + wl.tok_off);
   a.ws_lse = (float*)(ws + wl.lse_off);
   a.ws_o = (float*)(ws + wl.o_off);
-  a.ws_counter = (int32_t*)(ws + wl.counter_off);
-  a.ws_counter_len = wl.counter_len;
 
   cudaStream_t s = (cudaStream_t)stream;
   // Automatic choice: the tensor-core kernel when a request's rows fill a

@@ -34,13 +34,10 @@ struct VerifyArgs {
                                 //   merged: unsplit, empty or inconsistent request)
   float* ws_lse;                // [max_splits][total_q*heads]
   float* ws_o;                  // [max_splits][total_q*heads][512]
-  int32_t* ws_counter;          // [tiles] arrival counters (tensor-core path)
-  int64_t ws_counter_len;
 };
 
 struct WorkspaceLayout {
-  size_t tok_off, lse_off, o_off, counter_off, total;
-  int64_t counter_len;
+  size_t tok_off, lse_off, o_off, total;
 };
 
 WorkspaceLayout workspace_layout(int batch, int total_q, int heads, int max_splits);

@@ -93,6 +93,25 @@ def test_bits_config_sampled_tc(cid):
     compare_attention(st.out, st.lse, out, lse, rows=rows)
 
 
+def test_short_work_two_rounds_of_items():
+    """90 requests of one 128-row tile and 56-106 keys: the short-work
+    kernel variant (dry passes on a cluster's first item), with more items
+    than clusters, so clusters also run a second item without the dry pass."""
+    rng = np.random.default_rng(9)
+    prefix = [int(x) for x in rng.integers(40, 91, size=90)]
+    w = W.make_workload("rounds", 8, prefix, "uniform", [16] * 90, 65536, seed=9)
+    # the host's choice of the short-work variant: every tile against the
+    # whole kv_indices stays within 512 key blocks per cluster
+    tiles_ub = (w.total_q * w.heads + 127) // 128 + w.batch
+    assert tiles_ub * (sum(prefix) + w.total_q) <= 512 * 48 * 76
+    st = VerifyStep(w, path=abi.PATH_TC, fused=True)
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    out, lse = OracleRun(w).attention()
+    compare_attention(st.out, st.lse, out, lse)
+
+
 def test_bits_graph_capture_and_replay():
     w1 = W.make_workload("g", 8, [300, 1200, 77], "uniform", [16, 9, 30], 16384, seed=101)
     w2 = W.make_workload("g", 8, [300, 1200, 77], "uniform", [16, 9, 30], 16384, seed=202)

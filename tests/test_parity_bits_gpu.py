@@ -93,6 +93,47 @@ def test_bits_config_sampled_tc(cid):
     compare_attention(st.out, st.lse, out, lse, rows=rows)
 
 
+@pytest.mark.parametrize("n", [8192, 8193], ids=["at_limit", "over_limit"])
+def test_mask_tree_size_limit(n):
+    """A request of exactly MT_MAX_TREE = 8192 draft nodes packs bit for bit
+    (bytes and words); one node more is flagged MT_DEV_TREE_TOO_BIG and its
+    rows are left unwritten; the other request is still packed."""
+    sizes = [n, 5]
+    rng = np.random.default_rng(n)
+    parents = []
+    for k in sizes:
+        par = [-1] + [int(rng.integers(-1, i)) for i in range(1, k)]
+        parents.append(par)
+    w = W.make_workload("limit", 1, [16, 40], None, None, 16384, seed=3, parents=parents)
+    kv_indices, kv_indptr = oracle.kv_indices_build(w.prefix_indices, w.prefix_indptr,
+                                                    w.out_cache_loc, w.qo_indptr)
+    dev = torch.device("cuda")
+    par = w.parents.to(dev)
+    qptr = w.qo_indptr.to(dev)
+    kptr = torch.from_numpy(np.asarray(kv_indptr, dtype=np.int32)).to(dev)
+    B = w.batch
+    mi_ref, m_ref = oracle.tree_mask_pack(w.parents, w.qo_indptr, kv_indptr)
+    wi_ref, w_ref = oracle.tree_mask_pack_bits(w.parents, w.qo_indptr, kv_indptr)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    mask = torch.full((int(mi_ref[-1]),), 7, dtype=torch.uint8, device=dev)
+    mind = torch.empty(B + 1, dtype=torch.int64, device=dev)
+    abi.tree_mask_pack(par, qptr, kptr, mind, mask, status)
+    words = torch.full((int(wi_ref[-1]),), 7, dtype=torch.int32, device=dev)
+    wind = torch.empty(B + 1, dtype=torch.int64, device=dev)
+    abi.tree_mask_pack_bits(par, qptr, kptr, wind, words, status)
+    torch.cuda.synchronize()
+    assert (mind.cpu().numpy() == mi_ref).all() and (wind.cpu().numpy() == wi_ref).all()
+    m, wd = mask.cpu().numpy(), words.cpu().numpy().view(np.uint32)
+    if n <= 8192:
+        assert int(status.item()) == 0
+        assert (m == m_ref).all() and (wd == w_ref).all()
+    else:
+        assert int(status.item()) == abi.DEV_TREE_TOO_BIG
+        # request 0 untouched, request 1 packed
+        assert (m[:mi_ref[1]] == 7).all() and (m[mi_ref[1]:] == m_ref[mi_ref[1]:]).all()
+        assert (wd[:wi_ref[1]] == 7).all() and (wd[wi_ref[1]:] == w_ref[wi_ref[1]:]).all()
+
+
 def test_short_work_two_rounds_of_items():
     """90 requests of one 128-row tile and 56-106 keys: the short-work
     kernel variant (dry passes on a cluster's first item), with more items

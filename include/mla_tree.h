@@ -170,8 +170,10 @@ int tree_mask_pack_bits(const int32_t* parents, const int32_t* qo_indptr, const 
  * prefix_indptr and qo_indptr instead of reading kv_indptr. draft_kv and
  * kv_buf must be 16-byte aligned and draft_row_stride a multiple of 8
  * elements, else MT_EINVAL (the separate entry points take any alignment).
- * The paper's integration runs these steps in Python inside the serving
- * engine; here they are one kernel ahead of mla_tree_verify_bits.
+ * In "Deploying a Custom sm_120 Verify Kernel into Production" (section
+ * "The Context: Why This Deployment Matters") a separate Python backend
+ * module wires the kernel into the serving engine and prepares its inputs;
+ * here they are one kernel ahead of mla_tree_verify_bits.
  */
 int mla_tree_prepare(const mt_bf16* draft_kv, int64_t draft_row_stride,
                      const int32_t* out_cache_loc, const int32_t* prefix_indices,
@@ -300,8 +302,9 @@ int mla_tree_verify_masked(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_
  *   workspace: >= mla_tree_verify_validate_workspace_bytes(batch, total_q,
  *            heads, max_splits) bytes, 256-byte aligned.
  * Returns MT_EUNSUPPORTED when the tensor-core kernel cannot serve the call.
- * The paper's gate compared against a separate reference backend; here the
- * two paths are this library's own, written independently.
+ * The gate in "Deploying a Custom sm_120 Verify Kernel into Production"
+ * compared against the serving engine's own attention backend; here the two
+ * paths are this library's own, written independently.
  */
 size_t mla_tree_verify_validate_workspace_bytes(int batch, int total_q, int heads, int max_splits);
 int mla_tree_verify_validate(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,

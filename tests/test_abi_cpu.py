@@ -34,6 +34,42 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def _signatures():
+    """name -> (return type, [parameter types]) for every declaration."""
+    src = open(os.path.join(ROOT, "include", "mla_tree.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"\b(int|size_t|const char\*)\s+(\w+)\s*\(([^)]*)\)\s*;", src):
+        params = " ".join(params.split())
+        types = [] if params in ("", "void") else [p.rsplit(" ", 1)[0].strip() for p in params.split(",")]
+        out[name] = (ret, types)
+    return out
+
+
+def _ctype_of(c_type):
+    """The ctypes class a C parameter type is passed as."""
+    if "*" in c_type or c_type == "mt_stream_t":
+        return ctypes.c_void_p
+    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float}[c_type.replace("const ", "")]
+
+
+def test_binding_matches_header_signatures(lib):
+    """Every binding passes exactly the header's parameters, each with a
+    ctypes type of the right width, and reads the right return type."""
+    sigs = _signatures()
+    assert set(sigs) == set(abi.EXPORTS)
+    for name, (ret, types) in sigs.items():
+        fn = getattr(lib, name)
+        want_ret = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p}[ret]
+        assert fn.restype is want_ret, name
+        if name == "mla_tree_abi_version":
+            continue  # no parameters; ctypes keeps its default argtypes
+        assert fn.argtypes is not None and len(fn.argtypes) == len(types), (name, types)
+        for i, (got, c_type) in enumerate(zip(fn.argtypes, types)):
+            assert got is _ctype_of(c_type), (name, i, c_type, got)
+
+
 def test_version_and_status_strings(lib):
     assert lib.mla_tree_abi_version() == 100
     for code in (0, -1, -2, -3, -4):

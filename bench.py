@@ -6,9 +6,14 @@ KV index marshaling, tree-mask packing and tree-verify attention (with its
 split merge). By default the three marshaling steps run as one launch
 (mla_tree_prepare, which packs the mask in its bit form: one bit per (row,
 column)) ahead of mla_tree_verify_bits; --marshal separate --mask bytes runs
-the four separate calls with the byte mask. Default workload: 8 requests,
-prefixes U{1024..4096}, 16-node draft trees (branching <= 3), 8 heads,
-65536-slot pool.
+the four separate calls with the byte mask.
+
+Default workload (--config 5): the ragged mixed batch of 64 requests,
+prefixes floor(exp(U(ln 128, ln 131072))), tree sizes U{8..64} (even
+requests chains, odd ones random trees), 64 heads, 2^22-slot pool, run as
+one captured CUDA graph per step. --config 1..4 select the other four
+workloads (the live 9-node shape, 8 requests of 1k-4k keys, 32 requests of
+8192 keys, 4 requests of 200000 keys).
 
 Timing: the whole step is captured once as a CUDA graph (what a serving
 engine replays; there the verify kernel starts while the marshaling kernel
@@ -27,8 +32,11 @@ e2e = the same metric through the public API with host buffers: pinned
 host -> device copies of the step's inputs, the step's calls, and the device
 -> host read of out and lse, all inside the timed region.
 
---impl reference times the fp64 CPU oracle on the host cores on a bounded
-sample (one request of the same workload per step).
+The CPU baseline and --impl reference time the fp64 oracle on the host
+cores on a bounded sample of the same workload: whole requests (all their
+draft rows and heads, at least 256 rows in all) in a seeded random order,
+their index marshaling, mask packing and attention; value = the KV bytes of
+the requests done / the time taken.
 """
 from __future__ import annotations
 
@@ -47,6 +55,9 @@ sys.path.insert(0, ROOT)
 METRIC = "tree-verify MLA attention µs/call and KV GB/s (% of GB300 HBM roofline)"
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 FLUSH_BYTES = 256 << 20
+# timed steps per workload when --steps is not given: about a second of
+# device time in the timed region
+DEFAULT_STEPS = {1: 4000, 2: 4000, 3: 200, 4: 500, 5: 60}
 
 
 def _peaks():
@@ -139,13 +150,14 @@ def _kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def _traffic(key):
+    """DRAM bytes per launch of the verify call on one workload (key
+    "verify_c<N>") from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
-        e = t.get(kernel)
+        e = t.get(key)
         if e and e.get("source_hash") == _kernel_source_hash():
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -172,48 +184,70 @@ def whole_job_gbs(world, steps, kv_bytes, total_ms):
     return world * steps * kv_bytes / (total_ms * 1e-3) / 1e9
 
 
-def cpu_baseline(cid, budget_s, one_request=False, steps=None):
+class OracleSampler:
+    """The fp64 oracle on whole requests of one workload, in a seeded random
+    order. The pool with the draft rows scattered in is built once, before
+    any timing (a copy of the whole pool); each timed request then runs the
+    oracle's index marshaling, mask packing and attention of all its rows."""
+
+    def __init__(self, w, seed=0):
+        import numpy as np
+        import torch
+
+        import oracle
+
+        self.np, self.oracle = np, oracle
+        self.w = w
+        pool_bits = w.dense_pool().view(torch.int16).numpy().view(np.uint16)
+        dkv = w.draft_kv.view(torch.int16).numpy().view(np.uint16)
+        self.pool = oracle.draft_kv_scatter(pool_bits, dkv, w.out_cache_loc)
+        del pool_bits
+        self.q_bits = w.q.view(torch.int16).numpy().view(np.uint16)
+        self.qo = w.qo_indptr.numpy()
+        self.order = np.random.default_rng(seed).permutation(w.batch)
+        self.k = 0
+
+    def request(self):
+        """One request's oracle work; returns (KV bytes, rows)."""
+        w, o = self.w, self.oracle
+        b = int(self.order[self.k % w.batch])
+        self.k += 1
+        kv_indices, kv_indptr = o.kv_indices_build(w.prefix_indices, w.prefix_indptr,
+                                                   w.out_cache_loc, w.qo_indptr)
+        mask_indptr, mask = o.tree_mask_pack(w.parents, w.qo_indptr, kv_indptr)
+        rows = [(t, h) for t in range(self.qo[b], self.qo[b + 1]) for h in range(w.heads)]
+        o.verify_attention(self.q_bits, self.pool, kv_indices, kv_indptr, w.qo_indptr, mask,
+                           mask_indptr, w.heads, w.sm_scale, rows=rows)
+        return (w.prefix_lens[b] + w.tree_sizes[b]) * 1152, len(rows)
+
+    def run(self, budget_s=None, steps=None, min_rows=256):
+        """Requests until budget_s seconds have passed (and at least
+        min_rows rows are done), or exactly `steps` requests; returns
+        (GB/s, seconds, rows, requests)."""
+        done = rows = k = 0
+        t0 = time.perf_counter()
+        while True:
+            b, r = self.request()
+            done += b
+            rows += r
+            k += 1
+            el = time.perf_counter() - t0
+            if steps is not None:
+                if k >= steps:
+                    break
+            elif el >= budget_s and rows >= min_rows:
+                break
+        return done / el / 1e9, el, rows, k
+
+
+def cpu_baseline(w, budget_s):
     """Time the fp64 oracle on this host's cores; returns (GB/s, seconds, sample text)."""
-    import numpy as np
-    import torch
-
-    import oracle
-    from speculative_decode_mla_tree_gb300 import workloads as W
-
-    w = W.config(cid)
-    pool_bits = w.dense_pool().view(torch.int16).numpy().view(np.uint16)
-    q_bits = w.q.view(torch.int16).numpy().view(np.uint16)
-    dkv = w.draft_kv.view(torch.int16).numpy().view(np.uint16)
-    qo = w.qo_indptr.numpy()
-
-    def one_step(b=None):
-        pool = oracle.draft_kv_scatter(pool_bits, dkv, w.out_cache_loc)
-        kv_indices, kv_indptr = oracle.kv_indices_build(w.prefix_indices, w.prefix_indptr,
-                                                        w.out_cache_loc, w.qo_indptr)
-        mask_indptr, mask = oracle.tree_mask_pack(w.parents, w.qo_indptr, kv_indptr)
-        rows = None
-        if b is not None:
-            rows = [(t, h) for t in range(qo[b], qo[b + 1]) for h in range(w.heads)]
-        oracle.verify_attention(q_bits, pool, kv_indices, kv_indptr, w.qo_indptr, mask,
-                                mask_indptr, w.heads, w.sm_scale, rows=rows)
-        if b is None:
-            return w.kv_bytes()
-        return (w.prefix_lens[b] + w.tree_sizes[b]) * 1152
-
-    done, t0, k = 0, time.perf_counter(), 0
-    while True:
-        b = (k % w.batch) if one_request else None
-        done += one_step(b)
-        k += 1
-        el = time.perf_counter() - t0
-        if steps is not None and k >= steps:
-            break
-        if steps is None and el >= budget_s:
-            break
-    el = time.perf_counter() - t0
-    sample = ("%d oracle steps of %s" % (k, "one request each (all its rows)" if one_request
-                                          else "the whole batch"))
-    return done / el / 1e9, el, sample, k
+    s = OracleSampler(w)
+    gbs, el, rows, k = s.run(budget_s=budget_s)
+    sample = ("%d whole requests of the workload (%d rows of (draft node, head)) in a seeded random "
+              "order: index marshaling, mask packing and attention per request; the pool with the "
+              "draft rows scattered in is built once before timing" % (k, rows))
+    return gbs, el, sample, k
 
 
 def run_reference(args):
@@ -222,14 +256,17 @@ def run_reference(args):
         return 0
     cores = len(os.sched_getaffinity(0))
     from speculative_decode_mla_tree_gb300 import workloads as W
-    cpu_baseline(args.config, 0, one_request=True, steps=max(1, args.warmup))
-    gbs, el, sample, k = cpu_baseline(args.config, 0, one_request=True, steps=args.steps)
-    w = W.config(args.config)
-    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+    steps = args.steps
+    s = OracleSampler(W.config(args.config))
+    s.run(steps=args.warmup)
+    gbs, el, rows, k = s.run(steps=steps)
+    sample = ("%d steps of one whole request each (%d rows of (draft node, head) in all), requests "
+              "in a seeded random order after %d warm-up requests" % (k, rows, args.warmup))
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus, "steps": steps,
             "warmup": args.warmup, "ms_per_step": el / k * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": W.CONFIG_NAMES[args.config], "sample": "one request per step"},
+            "config": {"workload": W.CONFIG_NAMES[args.config], "sample": "one whole request per step"},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -266,7 +303,7 @@ def run_ours(args):
                     fused=fused, skip_prefix=args.skip_prefix)
     stream = torch.cuda.Stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2(v):
         flush.fill_(v)                                  # evict everything else from L2
@@ -393,7 +430,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, el, sample, k = cpu_baseline(args.config, args.cpu_seconds)
+        gbs, el, sample, k = cpu_baseline(w, args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                "sample": sample + " (%.1f s)" % el}
 
@@ -420,7 +457,7 @@ def run_ours(args):
                          "peak": hbm if bound == "hbm" else tf_burst,
                          "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                          "frac": (achieved_gbs / hbm) if bound == "hbm" else (achieved_tf / tf_burst),
-                         "traffic": _traffic("verify"), "peak_source": which,
+                         "traffic": _traffic("verify_c%d" % args.config), "peak_source": which,
                          "alg_bytes_per_launch": byts, "alg_flops_per_launch": flops,
                          "hbm_frac": achieved_gbs / hbm, "tensor_frac": achieved_tf / tf_burst},
             "cpu_baseline": cpu,
@@ -437,10 +474,11 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about a second of device time for the workload)")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--kv-layout", default="shuffled", choices=["shuffled", "contiguous", "paged64"],
@@ -458,6 +496,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.config]
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -187,9 +187,10 @@ int mla_tree_prepare(const mt_bf16* draft_kv, int64_t draft_row_stride,
 /*
  * Bytes of scratch workspace mla_tree_verify needs for these capacities
  * (max_splits 0 = the automatic choice mla_tree_verify makes for 0).
- * Holds per-split partial outputs (fp32 [splits][total_q*heads][512]), their
- * LSEs and per-request bookkeeping; the caller allocates it once, 256-byte
- * aligned, and may reuse it across calls on one stream.
+ * Holds the per-token split counts and, when max_splits > 1, the per-split
+ * partial outputs (fp32 [splits][total_q*heads][512]) and their LSEs; the
+ * caller allocates it once, 256-byte aligned, and may reuse it across calls
+ * on one stream.
  */
 size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int max_splits);
 
@@ -335,6 +336,10 @@ int mla_tree_verify_validate(const mt_bf16* q, const mt_bf16* kv_buf, int64_t nu
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing in it needs clearing). Calls that may overlap on the
  *     GPU -- unordered streams -- race on it; order them.
+ *   - The looked-up address is kept for the life of the process: after
+ *     cudaDeviceReset on a device, the library must not be used on that
+ *     device again (its cached per-device state, this address included,
+ *     would be stale).
  */
 #define MT_NOALLOC_SCRATCH_BYTES (64u << 20)
 int mla_tree_verify_noalloc(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_slots,

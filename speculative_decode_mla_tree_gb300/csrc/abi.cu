@@ -35,16 +35,21 @@ int auto_max_splits(int batch, int total_q, int heads, int num_sms) {
   return (int)s;
 }
 
+// Per-token split counts, then (only when a request may be split) the
+// per-split LSEs and fp32 partial outputs. With max_splits == 1 no kernel
+// writes or reads a partial: every row is finished in place.
 WorkspaceLayout workspace_layout(int batch, int total_q, int heads, int max_splits) {
+  (void)batch;
   WorkspaceLayout w;
   const size_t rows = (size_t)total_q * (size_t)heads;
+  const size_t parts = max_splits > 1 ? (size_t)max_splits : 0;
   size_t off = 0;
   w.tok_off = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1), 256);
   w.lse_off = off;
-  off = align_up(off + sizeof(float) * (size_t)max_splits * rows, 256);
+  off = align_up(off + sizeof(float) * parts * rows, 256);
   w.o_off = off;
-  off = align_up(off + sizeof(float) * (size_t)max_splits * rows * MT_D_V, 256);
+  off = align_up(off + sizeof(float) * parts * rows * MT_D_V, 256);
   w.total = off;
   return w;
 }

@@ -224,7 +224,8 @@ def make_workload(name, heads, prefix_lens, tree_rules, tree_sizes, num_slots, s
         prefix_indices=torch.cat(prefix_indices).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         out_cache_loc=torch.cat(out_cache_loc).to(torch.int32) if batch else torch.zeros(0, dtype=torch.int32),
         q=q, draft_kv=draft_kv, pool_slots=slots, pool_rows=pool_rows,
-        meta={"seed": seed, "rules": list(tree_rules) if tree_rules else None, "kv_layout": kv_layout},
+        meta={"seed": seed, "rules": list(tree_rules) if tree_rules else None, "kv_layout": kv_layout,
+              "latent_std": latent_std, "rope_std": rope_std},
     )
 
 
@@ -261,6 +262,76 @@ def config(cid: int, kv_layout: str = "shuffled") -> Workload:
         rules = ["chain" if b % 2 == 0 else "uniform" for b in range(64)]
         return make_workload("c5", 64, P, rules, n, 1 << 22, seed, **kw)
     raise ValueError(cid)
+
+
+def redraw(w: Workload, seed: int) -> Workload:
+    """New contents with the shapes of ``w``: the same batch, heads, pool
+    size, prefix lengths and tree sizes (so a CUDA graph captured on ``w``'s
+    buffers replays on it), with new tree parents drawn by the same rules,
+    new slots and new values, from ``seed``."""
+    m = w.meta
+    return make_workload(w.name, w.heads, w.prefix_lens, m["rules"], w.tree_sizes, w.num_slots,
+                         seed, latent_std=m.get("latent_std", 1.0), rope_std=m.get("rope_std", 1.0),
+                         sm_scale=w.sm_scale, kv_layout=m.get("kv_layout", "shuffled"))
+
+
+def _map_rows(w: Workload, q_fn, row_fn) -> Workload:
+    """A copy of ``w`` whose q, pool rows and draft rows are replaced by
+    q_fn(q) and row_fn(rows), computed in float32 and rounded to bf16."""
+    import dataclasses
+    q = q_fn(w.q.float()).to(torch.bfloat16)
+    return dataclasses.replace(w, q=q, pool_rows=row_fn(w.pool_rows.float()).to(torch.bfloat16),
+                               draft_kv=row_fn(w.draft_kv.float()).to(torch.bfloat16),
+                               meta=dict(w.meta))
+
+
+STRESS_KINDS = ("peaked", "cancel", "huge_v")
+
+
+def stress(w: Workload, kind: str) -> Workload:
+    """Input transforms that push the arithmetic of a verify kernel to the
+    edges of what bf16 inputs allow. Every factor is a power of two, so the
+    transformed values are exact in bf16.
+
+    peaked  every query value x8: scaled scores spread over tens of log2
+            units, so the softmax is dominated by a few keys per row.
+    cancel  key latent dims 256..511 copy dims 0..255; query dims 0..255
+            x16 and dims 256..511 their negation. The latent dot product is
+            exactly zero, but its two halves are large and of opposite sign,
+            so any kernel that rounds per-half partial scores loses the
+            (rope-only) score.
+    huge_v  key latent dims x2^17 and query latent dims x2^-17: the scores
+            are those of ``w``, while the values (latent dims) reach
+            several times 2^17, beyond the largest finite fp16 number.
+    """
+    if kind == "peaked":
+        return _map_rows(w, lambda q: q * 8.0, lambda r: r)
+
+    if kind == "cancel":
+        def qf(q):
+            q = q.clone()
+            q[..., :256] *= 16.0
+            q[..., 256:512] = -q[..., :256]
+            return q
+
+        def rf(r):
+            r = r.clone()
+            r[:, 256:512] = r[:, :256]
+            return r
+        return _map_rows(w, qf, rf)
+
+    if kind == "huge_v":
+        def qf(q):
+            q = q.clone()
+            q[..., :D_LATENT] *= 2.0 ** -17
+            return q
+
+        def rf(r):
+            r = r.clone()
+            r[:, :D_LATENT] *= 2.0 ** 17
+            return r
+        return _map_rows(w, qf, rf)
+    raise ValueError(kind)
 
 
 def small(seed=0, heads=8, batch=3, prefix=(5, 40, 130), tree=(4, 9, 17), rule="uniform",

@@ -161,6 +161,16 @@ def test_workspace_size_grows_with_splits(lib):
     assert lib.mla_tree_verify_workspace_bytes(8, 128, 8, 5000) == 0
 
 
+def test_unsplit_workspace_holds_no_partials(lib):
+    """max_splits 1 (and the automatic choice when the rows alone fill the
+    GPU, e.g. 32 requests x 64 nodes x 64 heads) needs only the per-token
+    split counts: no kernel writes a partial then."""
+    assert lib.mla_tree_verify_workspace_bytes(32, 2048, 64, 1) <= 2048 * 4 + 256
+    assert lib.mla_tree_verify_workspace_bytes(32, 2048, 64, 0) <= 2048 * 4 + 256
+    two = lib.mla_tree_verify_workspace_bytes(32, 2048, 64, 2)
+    assert two >= 2 * 2048 * 64 * 513 * 4
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(abi.MlaTreeError):

@@ -40,20 +40,47 @@ def _agree(out_a, lse_a, out_b, lse_b):
     assert rel.numel() == 0 or float(rel.max()) <= LSE_REL
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+PATHS = [pytest.param(abi.PATH_SIMT, id="simt"), pytest.param(abi.PATH_TC, id="tcgen05"),
+         pytest.param(abi.PATH_AUTO, id="auto")]
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_noalloc_matches_workspace_entry_point_twice(path):
+    """Two calls in a row: the first splits 1152 (node, head) rows over up to
+    16 splits per request, the second covers fewer tokens and splits, so it
+    runs on scratch that still holds the first call's partials and counts."""
     __graft_entry__.build()
-    cases = [(W.small(seed=41), 8),
-             (W.make_workload("na", 8, [900, 2500], "uniform", [16, 12], 8192, seed=42), 16)]
-    for w, splits in cases:            # two calls in a row, different shapes
-        st = VerifyStep(w, max_splits=splits, path=abi.PATH_SIMT)
+    cases = [(W.make_workload("na1", 16, [3000, 1200, 500], "uniform", [32, 16, 24], 16384, seed=42), 16),
+             (W.make_workload("na2", 8, [900, 300], "uniform", [16, 16], 8192, seed=43), 4)]
+    for w, splits in cases:
+        st = VerifyStep(w, max_splits=splits, path=path)
         st.run()                       # regular entry point with a caller workspace
         out = torch.empty_like(st.out)
         lse = torch.empty_like(st.lse)
-        rc = _noalloc_raw(st, out, lse, splits, abi.PATH_SIMT)
+        rc = _noalloc_raw(st, out, lse, splits, path)
         assert rc == abi.MT_OK, rc
         torch.cuda.synchronize()
         assert int(st.status.item()) == 0
         _agree(out, lse, st.out, st.lse)
+
+
+@pytest.mark.parametrize("splits", [1, 0], ids=["unsplit", "auto"])
+def test_noalloc_serves_unsplit_large_batches(splits):
+    """32 requests x 64 nodes x 64 heads (131072 rows): unsplit, and with the
+    automatic split choice (which is one split here), the call needs only
+    the per-token split counts and fits the built-in scratch."""
+    __graft_entry__.build()
+    w = W.config(3)
+    need = abi.mla_tree_verify_workspace_bytes(w.batch, w.total_q, w.heads, splits)
+    assert need <= abi.NOALLOC_SCRATCH_BYTES
+    st = VerifyStep(w, max_splits=splits, path=abi.PATH_TC)
+    st.run()
+    out = torch.empty_like(st.out)
+    lse = torch.empty_like(st.lse)
+    assert _noalloc_raw(st, out, lse, splits, abi.PATH_TC) == abi.MT_OK
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    _agree(out, lse, st.out, st.lse)
 
 
 def test_noalloc_rejects_requests_beyond_its_buffer():

@@ -201,6 +201,24 @@ size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int ma
 int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_splits, int path);
 
 /*
+ * Test facility for the kernels' failure detection (the paper has no
+ * counterpart; its validate gate is the nearest idea: "Deploying a Custom
+ * sm_120 Verify Kernel into Production", "The Validate Mode"). Every wait
+ * inside the tensor-core verify kernel is bounded; when one gives up, the
+ * kernel sets MT_DEV_TIMEOUT in dev_status, issues no further copy or MMA,
+ * drains what is in flight and exits, leaving the device usable.
+ *   wait_limit_ns: bound of every such wait, 0 = the default of 2 s.
+ *   drop_item:     -1 = off; else the kernel's copy engines issue nothing
+ *                  from its work item drop_item on (items number the
+ *                  (128-row tile, key split) pairs of a call from 0), so
+ *                  the waits on those keys run out.
+ * Process-wide: applies to every tensor-core verify call enqueued after it
+ * until it is called again with (-1, 0). Returns MT_EINVAL for
+ * drop_item < -1 or a negative limit. Not for production use.
+ */
+int mla_tree_test_wait_limits(int drop_item, int64_t wait_limit_ns);
+
+/*
  * Tree-verify attention ("Flipping the Switch", "The Long Road to Parity"
  * and "The Broader Context"; "Pivot to Live Cutover", "The Technical
  * Investigation" and "Input Knowledge Required"). For every request b, draft

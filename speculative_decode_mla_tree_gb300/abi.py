@@ -21,7 +21,7 @@ EXPORTS = ["mla_tree_abi_version", "mla_tree_status_string", "mla_tree_draft_kv_
            "mla_tree_kv_indices_build", "tree_mask_pack", "tree_mask_pack_bits", "mla_tree_prepare",
            "mla_tree_verify_workspace_bytes", "mla_tree_verify_launch_count", "mla_tree_verify",
            "mla_tree_verify_bits", "mla_tree_verify_masked", "mla_tree_verify_validate_workspace_bytes",
-           "mla_tree_verify_validate", "mla_tree_verify_noalloc"]
+           "mla_tree_verify_validate", "mla_tree_verify_noalloc", "mla_tree_test_wait_limits"]
 MT_ESCRATCH = -5
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -74,6 +74,8 @@ def load():
     lib.mla_tree_verify_validate.restype = I32
     lib.mla_tree_verify_validate.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                              P, P, P, SZ, I32, F32, P, P, P]
+    lib.mla_tree_test_wait_limits.restype = I32
+    lib.mla_tree_test_wait_limits.argtypes = [I32, I64]
     lib.mla_tree_verify_noalloc.restype = I32
     lib.mla_tree_verify_noalloc.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                             P, P, I32, I32, P, P]
@@ -178,6 +180,14 @@ def mla_tree_prepare(draft_kv, out_cache_loc, prefix_indices, prefix_indptr, qo_
         _ptr(mask_words, torch.int32, "mask_words"), mask_words.numel(),
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "mla_tree_prepare")
+
+
+def mla_tree_test_wait_limits(drop_item=-1, wait_limit_ns=0):
+    """Test facility: bound every wait of the tensor-core kernel by
+    wait_limit_ns (0 = the default) and make its copy engines issue nothing
+    from work item drop_item on (-1 = off). Process-wide."""
+    _check(load().mla_tree_test_wait_limits(int(drop_item), int(wait_limit_ns)),
+           "mla_tree_test_wait_limits")
 
 
 def mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits=0):

@@ -166,6 +166,12 @@ size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int ma
   return workspace_layout(batch, total_q, heads, max_splits).total;
 }
 
+int mla_tree_test_wait_limits(int drop_item, int64_t wait_limit_ns) {
+  if (drop_item < -1 || wait_limit_ns < 0) return MT_EINVAL;
+  set_tc_test_hooks(drop_item, (unsigned long long)wait_limit_ns);
+  return MT_OK;
+}
+
 int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_splits, int path) {
   if (batch < 0 || total_q < 0 || heads <= 0 || max_splits < 0 || max_splits > MT_MAX_SPLITS ||
       path < 0 || path > 2)

@@ -27,7 +27,7 @@ struct VerifyArgs {
   uint16_t* out;                // bf16 [total_q, heads, 512]
   float* lse;                   // fp32 [total_q, heads]
   int max_splits;               // capacity of the partial buffers
-  int partial_f16;              // split partials stored as fp16 (else fp32)
+  int partial_f16;              // split partials stored as fp16 (else fp32; the merge reads either)
   int32_t* status;
   // workspace views
   int32_t* ws_tok;              // [total_q] split count of each token's request (0: not
@@ -75,5 +75,8 @@ cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stream);
 // Kernels one tensor-core verify call launches (0 when that path cannot serve it).
 int verify_tc_launches(int batch, int total_q, int heads, int max_splits);
+// Test hooks of the tensor-core kernel's bounded waits (process-wide; see
+// mla_tree_test_wait_limits in the public header).
+void set_tc_test_hooks(int drop_item, unsigned long long limit_ns);
 
 }  // namespace mt

@@ -13,42 +13,46 @@
 // contiguous range of its key positions (a split). A tile is served by a
 // cluster of two CTAs on two SMs that split the head dims: CTA c holds
 // latent dims [256c, 256c+256) and rope dims [512+32c, 512+32c+32) of the
-// query tile and of every key row. Per block of BN = 48 key rows:
+// query tile and of every key row, and a 256-dim half of the output
+// accumulator O. The softmax is split by rows instead: CTA c owns tile rows
+// [64c, 64c+64). Per block of BN = 48 key rows:
 //
-//   query     per item: the rope half by TMA into shared memory, the
-//             256 latent dims by the sender warps straight into TMEM
 //   TMA       key-row halves by tile::gather4 through kv_indices, four rows
-//             per instruction, five stages in flight
+//             per instruction, several stages in flight
 //   tcgen05   S_c = Q_c K_c^T   (M=128, N=48, K=288) into TMEM
-//   DSMEM     each CTA rounds its partial S_c (scaled to the log2
-//             domain) to fp16 and sends it to its peer; both form
-//             fp16(S_0) + fp16(S_1) in fp32, so both hold bit-identical S
-//   softmax   mask bytes staged per block as bits, online max / sum in the
-//             log2 domain with lazy rescaling (the running max moves only
-//             when it grows by more than 8, i.e. a factor of 256)
+//   DSMEM     each CTA sends its fp32 partial scores of the rows the other
+//             CTA owns (64 rows x 48) to that CTA
+//   softmax   the owner adds the two fp32 partials (exact scores of its
+//             rows, in the log2 domain), applies the tree mask and runs the
+//             online softmax (two threads per row, 24 columns each; lazy
+//             rescaling: the running max moves only when it grows by more
+//             than 8, i.e. a factor of 256); it writes its rows of P (bf16)
+//             to its own TMEM and sends them, with the running max and
+//             sums, to the other CTA, which writes them into its TMEM (and
+//             rescales its half of those rows of O when the max moved)
 //   tcgen05   O_c += P V_c      (M=128, N=256, K=48) into TMEM; V_c is the
 //             same shared-memory key tile, read MN-major
 //
 // Why two CTAs: a 128-row fp32 accumulator for all 512 value dims is the
 // whole 256 KB of TMEM. Splitting the dims halves it and leaves TMEM room
 // for the query's latent half (so the QK MMAs read no query bytes from
-// shared memory, which at N = 48 would otherwise bound them) and two score
-// buffers; the exchange stays at the 48-column score block.
+// shared memory) and two score buffers. The scores cross between the CTAs
+// in fp32, so no partial is rounded below fp32 before the softmax.
 //
-// Roles per CTA (384 threads): warps 0-3 softmax / epilogue (one thread per
-// TMEM lane = tile row), warps 4-7 score senders (same lanes), warps 8-10
-// TMA producers (one warp alone issues tile::gather4 too slowly to keep
-// up), warp 11 MMA issuer
-// and TMEM owner. Every mbarrier wait is time-bounded: a timeout sets
-// MT_DEV_TIMEOUT, after which the CTA runs through to its exit without
-// waiting, draining its asynchronous copies and MMAs before releasing TMEM.
+// Roles per CTA (384 threads): in CTA c, warps 0-7 whose TMEM lane quarter
+// holds the own rows run the softmax and the own rows' epilogue; of the
+// other warps 0-7, warps 0-3 send partial scores and warps 4-7 receive P
+// and run those rows' epilogue; warps 8-10 are TMA producers (one warp
+// alone issues tile::gather4 too slowly to keep up); warp 11 issues the
+// MMAs and owns TMEM. Every mbarrier wait is time-bounded: a timeout sets
+// MT_DEV_TIMEOUT, after which no thread issues another copy, MMA or remote
+// store, every loop runs to its end (so no named barrier is left waiting)
+// and the copies and MMAs in flight are drained before TMEM is released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
-
-#include <cuda_fp16.h>
 
 #include "mt_common.cuh"
 #include "mt_internal.h"
@@ -61,46 +65,55 @@ using namespace sm100;
 
 constexpr int BM = 128;          // tile rows = TMEM lanes
 constexpr int BN = 48;           // key rows per block
+constexpr int kOwnRows = BM / 2; // rows whose softmax a CTA runs
+constexpr int kHalfCols = BN / 2;  // columns per softmax thread (two threads per row)
 constexpr int kGatherLanes = BN / 4;  // four-row groups per block (tile::gather4)
 constexpr int kProducers = 3;    // TMA producer warps (one warp issues about 37 ns per gather4)
-constexpr int kFirstProducer = 8;  // warps 0-3 softmax, 4-7 score senders
+constexpr int kFirstProducer = 8;
 constexpr int kMmaWarp = kFirstProducer + kProducers;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
-constexpr int kMaxBatch = 256;
+constexpr int kMaxBatch = 256;   // requests per launch (the plan lives in shared memory)
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
 constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
 constexpr int kSlotAhead = 2;    // key blocks whose slot numbers are in flight ahead of the gathers
-constexpr int kWarmBlocks = 512; // most key blocks per cluster (upper bound) for the dry-pass variant
+constexpr int kGroupsPerWarp = kGatherLanes / kProducers;
+static_assert(kGatherLanes % kProducers == 0, "groups per producer warp");
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kQRope = 0;                             // query rope half [128 rows x 64 B], 64B swizzle
-constexpr int kKV = kQRope + BM * 64;                 // key stages
+constexpr int kQTail = kQRope + BM * 64;              // query latent dims 224..255 of the CTA's half, same form
+constexpr int kKV = kQTail + BM * 64;                 // key stages
 constexpr int kKVLat = BN * 128;                      // one latent chunk of a stage
 constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 27648
 constexpr int kStages = 5;
-constexpr int kX = kKV + kStages * kKVStage;          // exchange: [XO0 | XP0 | XO1 | XP1]
-constexpr int kXRow = BN * 2 + 16;                    // fp16 scores of one row, padded: rows land on different banks
-constexpr int kXBytes = BM * kXRow;                   // one buffer (own XO or peer's XP)
+constexpr int kSX = kKV + kStages * kKVStage;         // the peer's fp32 partial scores of our rows, 2 buffers
+constexpr int kSXRow = BN * 4 + 16;                   // padded: rows land on different banks
+constexpr int kSXBytes = kOwnRows * kSXRow;
+constexpr int kPX = kSX + 2 * kSXBytes;               // the peer's P rows (+ running max, sums), 2 buffers
+constexpr int kPXRow = BN * 2 + 16;                   // P: 96 B; m at 96, l_0 at 100, l_1 at 104
+constexpr int kPXBytes = kOwnRows * kPXRow;
+constexpr int kMX = kPX + 2 * kPXBytes;               // half-row maxima [2][64][2] and sums [64][2]
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
-constexpr int kVis = kX + 4 * kXBytes;                // 2 x kVisNodes x 64-bit masks
+constexpr int kVis = kMX + (2 * kOwnRows * 2 + kOwnRows * 2) * 4;  // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
 constexpr int B_Q_FULL = 0;                     // query rope half landed (TMA)
 constexpr int B_QT_FULL = 1;                    // query latent half written to TMEM
 constexpr int B_Q_EMPTY = 2;                    // last QK of the item done
-constexpr int B_KV_FULL0 = 3;                   // kStages barriers each
-constexpr int B_KV_EMPTY0 = B_KV_FULL0 + kStages;
+constexpr int B_KV_FULL0 = 3;                   // kStages x kProducers: one per producer warp
+constexpr int B_KV_EMPTY0 = B_KV_FULL0 + kStages * kProducers;
 constexpr int B_S_FULL0 = B_KV_EMPTY0 + kStages;  // two each from here
 constexpr int B_S_EMPTY0 = B_S_FULL0 + 2;
-constexpr int B_X_FULL0 = B_S_EMPTY0 + 2;
-constexpr int B_X_FREE0 = B_X_FULL0 + 2;
-constexpr int B_P_FULL = B_X_FREE0 + 2;
-constexpr int B_O_DONE = B_P_FULL + 1;
-constexpr int B_O_FREE = B_O_DONE + 1;
+constexpr int B_SX_FULL0 = B_S_EMPTY0 + 2;
+constexpr int B_SX_FREE0 = B_SX_FULL0 + 2;
+constexpr int B_PX_FULL0 = B_SX_FREE0 + 2;
+constexpr int B_PX_FREE0 = B_PX_FULL0 + 2;
+constexpr int B_P_FULL0 = B_PX_FREE0 + 2;        // one per P buffer
+constexpr int B_O_DONE0 = B_P_FULL0 + 2;        // P.V done, one per P buffer it read
+constexpr int B_O_FREE = B_O_DONE0 + 2;
 constexpr int B_DRAIN = B_O_FREE + 1;
 constexpr int kNumBars = B_DRAIN + 1;
-constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count, B_DRY
-constexpr int B_DRY = (kMisc + 16 - kBars) / 8;       // never completes: the dry passes' waits and signals
+constexpr int kMisc = kBars + kNumBars * 8;           // tmem base, abort flag, item count, wait limit
 constexpr int kPlan = kMisc + 32;                     // per-request plan
 constexpr int kPlanStride = 9;                        // int32 words per request
 constexpr int kOrd = kPlan + kMaxBatch * kPlanStride * 4;   // request at each rank
@@ -108,37 +121,69 @@ constexpr int kOBase = kOrd + kMaxBatch * 4;          // first item of each rank
 constexpr int kSmemUsed = kOBase + (kMaxBatch + 1) * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kMisc % 8 == 0 && kBars + 8 * B_DRY + 8 <= kPlan, "B_DRY sits in the misc area");
-static_assert(2 * kXBytes >= BM * 128, "epilogue staging fits in one XO/XP pair");
 static_assert(BN % 16 == 0 && BN <= 64, "block width");
-static_assert(kQRope % 1024 == 0 && kKV % 1024 == 0 && kX % 1024 == 0 &&
-                  kKVStage % 1024 == 0 && kBars % 8 == 0,
+static_assert(kQRope % 1024 == 0 && kQTail % 1024 == 0 && kKV % 1024 == 0 && kKVStage % 1024 == 0 && kSX % 16 == 0 &&
+                  kPX % 16 == 0 && kSXRow % 16 == 0 && kPXRow % 16 == 0 && kBars % 8 == 0 &&
+                  kMisc % 8 == 0,
               "alignment");
 
-constexpr uint32_t kQTx = BM * 64;                    // query rope bytes per CTA per item
-constexpr uint32_t kKVTx = kKVStage;                  // key bytes per CTA per block
+constexpr uint32_t kQTx = 2 * BM * 64;                // query rope + latent-tail bytes per CTA per item
+constexpr uint32_t kKVTxWarp = kGroupsPerWarp * 4 * (4 * 128 + 64);  // key bytes per producer warp per block
+constexpr uint32_t kSXTx = kOwnRows * BN * 4;         // partial-score bytes into a CTA per block
+constexpr uint32_t kPXTx = kOwnRows * (BN * 2 + 12);  // P + m + l_0 + l_1 bytes into a CTA per block
+static_assert(kKVTxWarp * kProducers == (uint32_t)kKVStage, "stage bytes");
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns (512 x 128 lanes; lane = tile row):
 //   [0, 256)    O, this CTA's 256 value dims (fp32)
-//   [256, 384)  Q, this CTA's 256 latent query dims as bf16 pairs: QK's A
-//               operand (no shared-memory reads of Q per MMA)
+//   [256, 368)  Q, latent dims 0..223 of this CTA's half as bf16 pairs: QK's
+//               A operand for 14 of its 16 K steps (dims 224..255 and the
+//               rope come from shared memory)
 //   [384, 432)  S buffer 0, [448, 496) S buffer 1 (BN fp32 scores each)
-//   P (bf16 pairs, PV's A), one 8-column piece per 16 keys, in the gaps:
-//   [432, 448) and [496, 504)
+//   P (bf16 pairs, PV's A), two buffers, one 8-column piece per 16 keys:
+//   buffer 0 at [432, 448) and [496, 504), buffer 1 at [368, 384) and
+//   [504, 512). Two P buffers let P of block g+1 be written while the
+//   P.V of block g still reads P of block g.
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemQ = 256;
+constexpr int kQTmemSteps = 14;                       // QK K steps with A in TMEM
 constexpr uint32_t kTmemS = 384;                      // buffer b at kTmemS + 64 b
-__host__ __device__ constexpr uint32_t tmem_p_col(int t) { return t < 2 ? 432u + 8u * t : 496u; }
+__host__ __device__ constexpr uint32_t tmem_p_col(int pb, int t) {
+  return pb == 0 ? (t < 2 ? 432u + 8u * t : 496u) : (t < 2 ? 368u + 8u * t : 504u);
+}
 static_assert(BN == 48, "TMEM map holds 48-column score blocks and three P pieces");
+static_assert(kTmemQ + 8 * kQTmemSteps == 368, "Q ends where P buffer 1 starts");
 constexpr uint64_t kDrainNs = 100000000ull;           // 100 ms
-constexpr long long kIdleLimitCycles = 4000000000ll;  // about 2 s of SM clock with nothing to issue
+constexpr uint64_t kAbortSettleNs = 50000ull;         // after a give-up: let remote stores land
 
 // plan words
 enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI };
 
+// Optional pipeline trace for studying the kernel (off unless the library
+// is compiled with -DMT_TC_TRACE): %globaltimer at fixed points of the first
+// kTrBlocks key blocks of CTA 0, one thread per role, in
+// g_tc_trace[role][block][event]; read with mla_tree_tc_trace_read.
+enum { TR_PRODUCER, TR_MMA, TR_SENDER, TR_SOFTMAX, TR_RECEIVER, kTrRoles };
+constexpr int kTrBlocks = 1024, kTrEvents = 8;
+#ifdef MT_TC_TRACE
+__device__ unsigned long long g_tc_trace[kTrRoles][kTrBlocks][kTrEvents];
+#define TC_TRACE(on, role, blk, ev)                                         \
+  do {                                                                      \
+    if ((on) && blockIdx.x == 0 && (unsigned)(blk) < (unsigned)kTrBlocks)   \
+      g_tc_trace[role][blk][ev] = global_timer_ns();                        \
+  } while (0)
+#else
+#define TC_TRACE(on, role, blk, ev) \
+  do {                              \
+  } while (0)
+#endif
+
 struct TcParams {
-  VerifyArgs a;
+  VerifyArgs a;          // one chunk of at most kMaxBatch requests (indptrs offset to it)
   int nclusters;
+  int first_chunk;       // the chunk holding request 0 / the last request: bounds of the
+  int last_chunk;        //   token range whose split counts this launch publishes
+  int drop_item;         // test hook: producers issue nothing from this item on (-1: off)
+  unsigned long long limit_ns;  // bound of every wait
 };
 
 struct Item {
@@ -198,8 +243,9 @@ __device__ __forceinline__ long long warp_sum(long long v) {
 // Split length: a quarter of one cluster's fair share of (tile x key) work,
 // at least kMinChunk keys, so that a long request is cut into enough items
 // for every cluster to get several and the last round stays short.
-__device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* ord, int* obase,
-                           int* total_items, int lane, bool publish) {
+__device__ void build_plan(const TcParams& p, int* plan, int* ord, int* obase, int* total_items,
+                           int lane, bool publish) {
+  const VerifyArgs& a = p.a;
   const int H = a.heads;
   long long units = 0;
   for (int b = lane; b < a.batch; b += 32) {
@@ -219,7 +265,7 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
     units += (long long)tiles * g.L;
   }
   units = warp_sum(units);
-  const long long nc = nclusters > 0 ? nclusters : 1;
+  const long long nc = p.nclusters > 0 ? p.nclusters : 1;
   long long chunk = (units + 4 * nc - 1) / (4 * nc);
   if (chunk < kMinChunk) chunk = kMinChunk;
   chunk = (chunk + BN - 1) / BN * BN;
@@ -281,10 +327,15 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
     if (r < a.batch) obase[r] = carry + incl - items;
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  // tokens of inconsistent requests (or outside every request) are not merged
+  // tokens of this launch's range that no consistent request covers (an
+  // inconsistent request, or outside every request) are not merged
   if (publish) {
     __syncwarp();
-    for (int tk = lane; tk < a.total_q; tk += 32) {
+    int tlo = p.first_chunk ? 0 : a.qo_indptr[0];
+    int thi = p.last_chunk ? a.total_q : a.qo_indptr[a.batch];
+    tlo = max(0, tlo);
+    thi = min(a.total_q, thi);
+    for (int tk = tlo + lane; tk < thi; tk += 32) {
       int covered = 0;
       for (int b = 0; b < a.batch && !covered; ++b) {
         const int* pr = plan + b * kPlanStride;
@@ -300,16 +351,13 @@ __device__ void build_plan(const VerifyArgs& a, int nclusters, int* plan, int* o
 }
 
 // kBits: the tree mask is in the bit form (rows of ceil(L / 32) words)
-// kWarm: dry passes that load the softmax and sender loops' code before the
-// first scores arrive (worth it when each cluster has few blocks to do)
 // kSkip: prefix columns are visible and their mask entries are not read
-template <bool kBits, bool kWarm, bool kSkip>
+template <bool kBits, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ TcParams p,
                      const __grid_constant__ CUtensorMap tm_qrope,
                      const __grid_constant__ CUtensorMap tm_kvlat,
                      const __grid_constant__ CUtensorMap tm_kvrope) {
-  static_assert(kBits || !kWarm, "the softmax dry pass reads the bit-form mask");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -319,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t cta = cluster_ctarank();
   const uint32_t peer = cta ^ 1u;
   const int cluster_id = blockIdx.x >> 1;
+  const uint64_t limit = p.limit_ns;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kMisc + 4);
@@ -327,30 +376,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* ord = reinterpret_cast<int*>(sm + kOrd);
   int* obase = reinterpret_cast<int*>(sm + kOBase);
   uint64_t* vis = reinterpret_cast<uint64_t*>(sm + kVis);
+  float* mxs = reinterpret_cast<float*>(sm + kMX);               // [2][64][2] half-row maxima
+  float* lxs = mxs + 2 * kOwnRows * 2;                           // [64][2] half-row sums
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    mbar_init(&bars[B_QT_FULL], 128);
+    mbar_init(&bars[B_QT_FULL], 128 + 64);            // softmax threads + senders
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[B_KV_FULL0 + s], 1);
+      for (int w = 0; w < kProducers; ++w) mbar_init(&bars[B_KV_FULL0 + s * kProducers + w], 1);
       mbar_init(&bars[B_KV_EMPTY0 + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[B_S_FULL0 + s], 1);
-      mbar_init(&bars[B_S_EMPTY0 + s], 128);
+      mbar_init(&bars[B_S_EMPTY0 + s], 128 + 64);     // softmax threads + senders
+      mbar_init(&bars[B_SX_FULL0 + s], 1);            // armed once per block, + the peer's bytes
+      mbar_init(&bars[B_SX_FREE0 + s], 4);            // the peer's four softmax warps
+      mbar_init(&bars[B_PX_FULL0 + s], 1);
+      mbar_init(&bars[B_PX_FREE0 + s], 2);            // the peer's two receiver warps
     }
-    mbar_init(&bars[B_P_FULL], 128);
-    mbar_init(&bars[B_O_DONE], 1);
-    mbar_init(&bars[B_O_FREE], 128);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[B_X_FULL0 + x], 128);  // own senders (one with expect_tx) + the peer's bytes
-      mbar_init(&bars[B_X_FREE0 + x], 8);    // own four softmax warps and the peer's, one arrival each
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[B_P_FULL0 + s], 128 + 64);      // softmax threads + receivers
+      mbar_init(&bars[B_O_DONE0 + s], 1);
     }
+    mbar_init(&bars[B_O_FREE], 128 + 64);
     mbar_init(&bars[B_DRAIN], 1);
-    if (kWarm) mbar_init(&bars[B_DRY], (1 << 20) - 1);  // the largest count: its first phase never completes
     *abort = 0;
     fence_mbar_init_cluster();
+    // the first two blocks' exchange buffers are expected before any
+    // arrival from the peer is possible (the peer waits for the cluster
+    // barrier below)
+    for (int s = 0; s < 2; ++s) {
+      mbar_arrive_expect_tx(&bars[B_SX_FULL0 + s], kSXTx);
+      mbar_arrive_expect_tx(&bars[B_PX_FULL0 + s], kPXTx);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -361,34 +420,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_kvlat);
     prefetch_tmap(&tm_kvrope);
   }
-  // the last CTA publishes the split counts: with fewer items than clusters it
-  // has none of its own, so the extra stores delay no item
   // Launched as a programmatic dependent of the kernel before it (the
   // marshaling of the same step): the set-up above overlaps that kernel's
   // tail; nothing it writes is read before it has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (warp == 0)
-    build_plan(a, p.nclusters, plan, ord, obase, total_items_s, lane, blockIdx.x == gridDim.x - 1);
+  // the last CTA publishes the split counts: with fewer items than clusters it
+  // has none of its own, so the extra stores delay no item
+  if (warp == 0) build_plan(p, plan, ord, obase, total_items_s, lane, blockIdx.x == gridDim.x - 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   // The peer's barriers must exist before anyone touches them remotely: every
-  // thread arrives here, and only the softmax warps (the only ones that
-  // reach into the peer) wait before their first remote access.
+  // thread arrives here, and the warps that reach into the peer wait before
+  // their first remote access; the others wait at the end.
   cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   const int total_items = *total_items_s;
+  const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+  const bool own_quarter = (uint32_t)(q4 >> 1) == cta;
+  const int64_t q_rows = (int64_t)a.total_q * H;
+  const int64_t R = q_rows;
 
   if (warp >= kFirstProducer && warp < kFirstProducer + kProducers) {
     // ------------------------------------------------------------ producers
     // kProducers warps share every block's gathers: warp pw issues the
     // four-row groups [pw * kGroupsPerWarp, (pw + 1) * kGroupsPerWarp), one
-    // group per lane. The first producer warp also loads the query tile and
-    // arms each stage's barrier with the whole stage's byte count (bytes of
-    // the other warps may land before that arrival; the phase cannot
-    // complete without it).
-    constexpr int kGroupsPerWarp = kGatherLanes / kProducers;
-    static_assert(kGatherLanes % kProducers == 0, "groups per producer warp");
+    // group per lane, and completes its own barrier of the stage (so it can
+    // drain exactly the copies it issued). The first producer warp also
+    // loads the query tile's rope half.
     const int pw = warp - kFirstProducer;
     const int grp = pw * kGroupsPerWarp + lane;
     const bool gathers = lane < kGroupsPerWarp;
@@ -424,16 +483,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows[e] = slot;
       }
     };
-    for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
+    bool stop = false;
+    for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items && !stop;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
+      if (id == p.drop_item) break;  // test hook: the waits on this item's keys must give up
       const Item it = decode_item(plan, ord, obase, a.batch, id);
       const int qrow = it.q0 * H + it.row0;
-      if (pw == 0 && lane == 0) {
-        mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort);
-        mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTx);
-        tma_load_2d(sm + kQRope, &tm_qrope, 512 + 32 * (int)cta, qrow, &bars[B_Q_FULL]);
+      if (pw == 0) {
+        int ok = 0;
+        if (lane == 0 && mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort, limit) && !*abort) {
+          mbar_arrive_expect_tx(&bars[B_Q_FULL], kQTx);
+          tma_load_2d(sm + kQRope, &tm_qrope, 512 + 32 * (int)cta, qrow, &bars[B_Q_FULL]);
+          tma_load_2d(sm + kQTail, &tm_qrope, 256 * (int)cta + 224, qrow, &bars[B_Q_FULL]);
+          ok = 1;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // given up: issue nothing more
+        ++qi;
       }
-      ++qi;
       // Slot numbers run kSlotAhead blocks ahead of the gathers. The block
       // loop is unrolled by kSlotAhead so that ring entry u always holds the
       // slots of blocks u, u + kSlotAhead, ...: an entry is reloaded right
@@ -448,40 +514,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         live[d] = 0;
         if (gathers && d < it.nblocks) load_rows(it, d, ring[d], live[d]);
       }
-      for (int blk0 = 0; blk0 < it.nblocks; blk0 += kSlotAhead) {
+      for (int blk0 = 0; blk0 < it.nblocks && !stop; blk0 += kSlotAhead) {
 #pragma unroll
         for (int u = 0; u < kSlotAhead; ++u) {
           const int blk = blk0 + u;
-          if (blk < it.nblocks) {
+          if (blk < it.nblocks && !stop) {
             const int s = kb % kStages;
             uint8_t* st = sm + kKV + s * kKVStage;
+            uint64_t* full = &bars[B_KV_FULL0 + s * kProducers + pw];
+            int go = 0;
             if (lane == 0) {
-              mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort);
-              if (pw == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL0 + s], kKVTx);
+              go = mbar_wait<false>(&bars[B_KV_EMPTY0 + s], ((kb / kStages) & 1) ^ 1, abort, limit) &&
+                   !*abort;
+              if (go) mbar_arrive_expect_tx(full, kKVTxWarp);
             }
-            __syncwarp();
+            go = __shfl_sync(0xffffffffu, go, 0);
+            TC_TRACE(pw == 0 && lane == 0, TR_PRODUCER, kb, 0);
+            if (!go) {  // given up: issue nothing more
+              stop = true;
+              break;
+            }
             if (gathers) {
               int rows[4];
               take_rows(ring[u], live[u], rows);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 tma_gather4(st + k * kKVLat + grp * 512, &tm_kvlat, 256 * (int)cta + 64 * k,
-                            rows[0], rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
+                            rows[0], rows[1], rows[2], rows[3], full);
               tma_gather4(st + 4 * kKVLat + grp * 256, &tm_kvrope, 512 + 32 * (int)cta, rows[0],
-                          rows[1], rows[2], rows[3], &bars[B_KV_FULL0 + s]);
+                          rows[1], rows[2], rows[3], full);
               live[u] = 0;
               if (blk + kSlotAhead < it.nblocks) load_rows(it, blk + kSlotAhead, ring[u], live[u]);
             }
             __syncwarp();
+            TC_TRACE(pw == 0 && lane == 0, TR_PRODUCER, kb, 1);
             ++kb;
           }
         }
       }
     }
-    if (pw == 0 && lane == 0) {  // every copy this CTA issued has landed before it may exit
-      if (qi > 0) mbar_drain(&bars[B_Q_FULL], (qi - 1) & 1, kDrainNs);
+    if (lane == 0) {  // every copy this warp issued has landed before the CTA may exit
+      if (pw == 0 && qi > 0) mbar_drain(&bars[B_Q_FULL], (qi - 1) & 1, kDrainNs);
       for (uint32_t k = kb >= kStages ? kb - kStages : 0; k < kb; ++k)
-        mbar_drain(&bars[B_KV_FULL0 + (k % kStages)], (k / kStages) & 1, kDrainNs);
+        mbar_drain(&bars[B_KV_FULL0 + (k % kStages) * kProducers + pw], (k / kStages) & 1, kDrainNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -490,43 +565,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, 256, 0, 1);
       const uint32_t qrope = smem_u32(sm + kQRope);
+      const uint32_t qtail = smem_u32(sm + kQTail);
       const uint32_t kvbase = smem_u32(sm + kKV);
-      for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
-         id = item_of(++rnd, cluster_id, p.nclusters)) {
+      bool dead = false;
+      for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items && !dead;
+           id = item_of(++rnd, cluster_id, p.nclusters)) {
         const Item it = decode_item(plan, ord, obase, a.batch, id);
-        mbar_wait<false>(&bars[B_Q_FULL], qi & 1, abort);
-        mbar_wait<false>(&bars[B_QT_FULL], qi & 1, abort);
+        if (!mbar_wait<false>(&bars[B_Q_FULL], qi & 1, abort, limit) ||
+            !mbar_wait<false>(&bars[B_QT_FULL], qi & 1, abort, limit))
+          break;
         ++qi;
         tc_fence_after();
         const uint32_t kb0 = kb;
         // Two independent streams, polled without blocking: S_j = Q K_j^T
-        // as soon as key block j has landed and a score buffer is free
-        // (both are read by the senders early), and O += P_j V_j as soon as
-        // the softmax has written P_j. Waiting for P_j before issuing the
-        // next scores would tie every block to the softmax two blocks back.
+        // as soon as key block j has landed and a score buffer is free, and
+        // O += P_j V_j as soon as P_j is written (own rows by the softmax,
+        // the other rows by the receivers). Waiting for P_j before issuing
+        // the next scores would tie every block to the softmax two blocks back.
         int nq = 0, np = 0;
         bool ofree = false;
-        long long idle_since = 0;
+        uint64_t idle_since = 0;
         while (np < it.nblocks) {
           bool did = false;
           if (nq < it.nblocks) {
             const uint32_t kbi = kb0 + nq;
-            const uint32_t s = kbi % kStages, sb = sc & 1;
-            if (mbar_test_wait(&bars[B_KV_FULL0 + s], (kbi / kStages) & 1) &&
-                mbar_test_wait(&bars[B_S_EMPTY0 + sb], ((sc >> 1) & 1) ^ 1)) {
+            const uint32_t s = kbi % kStages, sb = sc & 1, ph = (kbi / kStages) & 1;
+            bool landed = mbar_test_wait(&bars[B_S_EMPTY0 + sb], ((sc >> 1) & 1) ^ 1);
+#pragma unroll
+            for (int w = 0; w < kProducers; ++w)
+              landed = landed && mbar_test_wait(&bars[B_KV_FULL0 + s * kProducers + w], ph);
+            if (landed) {
               tc_fence_after();
               const uint32_t stg = kvbase + s * kKVStage;
               const uint32_t d = tmem + kTmemS + 64 * sb;
 #pragma unroll
-              for (int k = 0; k < 16; ++k)  // latent dims 16k.. from TMEM, keys' 64-dim chunk k/4
+              for (int k = 0; k < kQTmemSteps; ++k)  // latent dims 16k.. from TMEM, keys' 64-dim chunk k/4
                 mma_bf16_ts(d, tmem + kTmemQ + 8 * k,
                             smem_desc(stg + (k >> 2) * kKVLat + 32 * (k & 3), 16, 1024, kSwizzle128B),
                             idesc_qk, k != 0);
+#pragma unroll
+              for (int k = kQTmemSteps; k < 16; ++k)  // latent dims 224..255 from shared memory
+                mma_bf16_ss(d, smem_desc(qtail + 32 * (k - kQTmemSteps), 16, 512, kSwizzle64B),
+                            smem_desc(stg + (k >> 2) * kKVLat + 32 * (k & 3), 16, 1024, kSwizzle128B),
+                            idesc_qk, 1);
 #pragma unroll
               for (int t = 0; t < 2; ++t)
                 mma_bf16_ss(d, smem_desc(qrope + 32 * t, 16, 512, kSwizzle64B),
                             smem_desc(stg + 4 * kKVLat + 32 * t, 16, 512, kSwizzle64B), idesc_qk, 1);
               mma_commit(&bars[B_S_FULL0 + sb]);
+              TC_TRACE(true, TR_MMA, kbi, 0);
               ++sc;
               if (++nq == it.nblocks) mma_commit(&bars[B_Q_EMPTY]);  // last use of Q
               did = true;
@@ -534,17 +621,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (np < nq) {
             if (!ofree) ofree = mbar_test_wait(&bars[B_O_FREE], (ii & 1) ^ 1);
-            if (ofree && mbar_test_wait(&bars[B_P_FULL], pc & 1)) {
+            const uint32_t pb = pc & 1;
+            if (ofree && mbar_test_wait(&bars[B_P_FULL0 + pb], (pc >> 1) & 1)) {
               tc_fence_after();
               const uint32_t s = (kb0 + np) % kStages;
               const uint32_t stg = kvbase + s * kKVStage;
 #pragma unroll
               for (int t = 0; t < BN / 16; ++t)
-                mma_bf16_ts(tmem + kTmemO, tmem + tmem_p_col(t),
+                mma_bf16_ts(tmem + kTmemO, tmem + tmem_p_col(pb, t),
                             smem_desc(stg + t * 2048, kKVLat, 1024, kSwizzle128B), idesc_pv,
                             (np | t) != 0);
               mma_commit(&bars[B_KV_EMPTY0 + s]);
-              mma_commit(&bars[B_O_DONE]);
+              mma_commit(&bars[B_O_DONE0 + pb]);
+              TC_TRACE(true, TR_MMA, kb0 + np, 1);
               ++pc;
               ++np;
               did = true;
@@ -553,11 +642,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (did) {
             idle_since = 0;
           } else {  // nothing ready: bounded like every other wait
-            if (*abort) break;
-            const long long now = clock64();
+            if (*abort) {
+              dead = true;
+              break;
+            }
+            const uint64_t now = global_timer_ns();
             if (idle_since == 0) idle_since = now;
-            else if (now - idle_since > kIdleLimitCycles) {
+            else if (now - idle_since > limit) {
               *abort = 1;
+              dead = true;
               break;
             }
           }
@@ -568,42 +661,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[B_DRAIN]);  // everything issued has completed before TMEM is freed
       mbar_drain(&bars[B_DRAIN], 0, kDrainNs);
     }
-  } else if (warp >= 4) {
+  } else if (!own_quarter && warp < 4) {
     // ------------------------------------------------------------ score senders
-    // Thread r owns row r (TMEM lane r). As soon as the scores of a block are
-    // in TMEM it reads its row of this CTA's partial S_c = Q_c K_c^T, scales
-    // it into the log2 domain, rounds it to fp16 and writes it twice: into
-    // the own buffer XO and, by st.async, into the peer's buffer XP, whose
-    // arrival completes the peer's X_FULL. Both CTAs then form
-    // fp32(XO) + fp32(XP) with the same two fp16 terms, so they hold the
-    // same scores bit for bit. Working ahead of the softmax warps, the
-    // senders overlap a block's exchange with the previous block's softmax.
-    const int r = tid - 128;
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    // Thread rp owns tile row 64 (1 - c) + rp, which the peer's softmax
+    // runs. Per item it writes that row's latent query half into TMEM (QK's
+    // A operand); per block it reads the row's fp32 partial score from TMEM,
+    // scales it into the log2 domain and stores it into the peer's SX
+    // buffer, whose arrival completes the peer's SX_FULL.
+    const int rp = (q4 - 2 * (int)(1u - cta)) * 32 + lane;
+    const int r = 64 * (int)(1u - cta) + rp;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float scale2 = a.sm_scale * kLog2e;
-    const uint32_t xp_peer0 = mapa(smem_u32(sm + kX + kXBytes + r * kXRow), peer);
-    const uint32_t xfull_peer0 = mapa(smem_u32(&bars[B_X_FULL0]), peer);
+    const uint32_t sx_peer = mapa(smem_u32(sm + kSX + rp * kSXRow), peer);
+    const uint32_t sxfull_peer0 = mapa(smem_u32(&bars[B_SX_FULL0]), peer);
+    const bool tr = warp == (int)(2 - 2 * cta) && lane == 0;  // traced thread
+    (void)tr;
     uint32_t g = 0, qi = 0;
-    const int64_t q_rows = (int64_t)a.total_q * H;
+    bool dead = false;
     cluster_wait();  // the peer's barriers are initialised
     for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
       const Item it = decode_item(plan, ord, obase, a.batch, id);
       {
         // Row r of the query tile, this CTA's 256 latent dims, into TMEM as
-        // bf16 pairs (QK's A operand) once the previous item's last QK is done.
-        // Rows past the last query row read as zeros.
+        // bf16 pairs once the previous item's last QK is done. Rows past
+        // the last query row read as zeros.
         const int64_t qrow = (int64_t)it.q0 * H + it.row0 + r;
         const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * kDqk + 256 * cta);
         const bool in = qrow < q_rows;
-        mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort);
+        if (!dead) dead = !mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort, limit);
         ++qi;
         tc_fence_after();
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        {  // dims 0..127, then 128..223
           uint4 v[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = in ? __ldg(src + 16 * half + k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 16; ++k) v[k] = in ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
           uint32_t w0[32], w1[32];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -611,101 +703,254 @@ __global__ void __launch_bounds__(kThreads, 1)
             w1[4 * k] = v[8 + k].x; w1[4 * k + 1] = v[8 + k].y;
             w1[4 * k + 2] = v[8 + k].z; w1[4 * k + 3] = v[8 + k].w;
           }
-          tmem_st32(tmem + lane_base + kTmemQ + 64 * half, w0);
-          tmem_st32(tmem + lane_base + kTmemQ + 64 * half + 32, w1);
+          tmem_st32(tmem + lane_base + kTmemQ, w0);
+          tmem_st32(tmem + lane_base + kTmemQ + 32, w1);
+        }
+        {
+          uint4 v[12];
+#pragma unroll
+          for (int k = 0; k < 12; ++k) v[k] = in ? __ldg(src + 16 + k) : make_uint4(0, 0, 0, 0);
+          uint32_t w0[32], w1[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            w0[4 * k] = v[k].x; w0[4 * k + 1] = v[k].y; w0[4 * k + 2] = v[k].z; w0[4 * k + 3] = v[k].w;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            w1[4 * k] = v[8 + k].x; w1[4 * k + 1] = v[8 + k].y;
+            w1[4 * k + 2] = v[8 + k].z; w1[4 * k + 3] = v[8 + k].w;
+          }
+          tmem_st32(tmem + lane_base + kTmemQ + 64, w0);
+          tmem_st16(tmem + lane_base + kTmemQ + 96, w1);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[B_QT_FULL]);
       }
-      // kWarm: the first item starts with a dry pass (blk = -1) as in the
-      // softmax warps: its waits and signals go to B_DRY, it reads O's
-      // columns (not written before the first P.V), writes only the own
-      // exchange buffer (rewritten before the softmax may read it) and
-      // sends nothing.
-      const int warm = (kWarm && rnd == 0) ? 1 : 0;
-      g -= warm;
-      for (int blk = -warm; blk < it.nblocks; ++blk, ++g) {
-        const bool dry = kWarm && blk < 0;
-        const uint32_t b = g & 1;
-        mbar_wait<false>(&bars[dry ? B_DRY : B_S_FULL0 + b], (g >> 1) & 1, abort);
+      for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
+        const uint32_t b = g & 1, ph = (g >> 1) & 1;
+        if (!dead) dead = !mbar_wait<false>(&bars[B_S_FULL0 + b], ph, abort, limit);
+        TC_TRACE(tr, TR_SENDER, g, 0);
         tc_fence_after();
         uint32_t s0[32], s1[16];
-        const uint32_t tsrc = tmem + lane_base + (dry ? kTmemO : kTmemS + 64 * b);
+        const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b;
         tmem_ld32(tsrc, s0);
         tmem_ld16(tsrc + 32, s1);
         tc_fence_before();
-        mbar_arrive(&bars[dry ? B_DRY : B_S_EMPTY0 + b]);  // the score buffer may take block g+2
-        uint32_t h[BN / 2];
+        mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
+        float x[BN];
 #pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          const uint32_t u0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
-          const uint32_t u1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-          // clamp to the finite fp16 range (scores that large saturate the
-          // softmax either way)
-          const float x0 = fminf(fmaxf(__uint_as_float(u0) * scale2, -65504.f), 65504.f);
-          const float x1 = fminf(fmaxf(__uint_as_float(u1) * scale2, -65504.f), 65504.f);
-          const __half2 v = __floats2half2_rn(x0, x1);
-          h[c] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        // both halves of buffer pair b are free: our softmax rows and the
-        // peer's have read block g-2
-        mbar_wait<true>(&bars[dry ? B_DRY : B_X_FREE0 + b], (((g >> 1) & 1) ^ 1) | (dry ? 1u : 0u), abort);
-        uint8_t* xo = sm + kX + 2 * b * kXBytes + r * kXRow;
-        const uint32_t dst = xp_peer0 + 2 * b * kXBytes;
-        const uint32_t bar = xfull_peer0 + 8 * b;
+        for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]) * scale2;
+        // the peer's softmax has read block g-2 from this buffer
+        if (!dead) dead = !mbar_wait<false>(&bars[B_SX_FREE0 + b], ph ^ 1, abort, limit);
+        if (!dead && !*abort) {
+          const uint32_t dst = sx_peer + b * kSXBytes;
+          const uint32_t bar = sxfull_peer0 + 8 * b;
 #pragma unroll
-        for (int q = 0; q < BN / 8; ++q) {
-          *reinterpret_cast<uint4*>(xo + 16 * q) = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-          if (!dry) st_async_v4(dst + 16 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3], bar);
+          for (int q = 0; q < BN / 4; ++q)
+            st_async_v4(dst + 16 * q, __float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
+                        __float_as_uint(x[4 * q + 2]), __float_as_uint(x[4 * q + 3]), bar);
         }
-        // own row written; r == 0 also arms the barrier for the peer's bytes
-        uint64_t* xfull = &bars[dry ? B_DRY : B_X_FULL0 + b];
-        if (r == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(BM * BN * 2));
-        else mbar_arrive(xfull);
+        TC_TRACE(tr, TR_SENDER, g, 1);
       }
     }
-  } else {
-    // ------------------------------------------------------------ softmax, epilogue
-    // Block g's scores come from buffer pair g & 1 (XO: ours, XP: the
-    // peer's), two pairs so the senders may fill block g+1 while the rows
-    // are still on block g.
-    const int r = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (!own_quarter) {
+    // ------------------------------------------------------------ P receivers
+    // Thread rp owns tile row 64 (1 - c) + rp. Per block it takes that row's
+    // P (bf16), running max and half sums from the peer's message, rescales
+    // this CTA's half of the row of O when the max moved, and writes P into
+    // TMEM for the P.V MMA. After an item it writes the row's output half.
+    const int rp = (q4 - 2 * (int)(1u - cta)) * 32 + lane;
+    const int r = 64 * (int)(1u - cta) + rp;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO;
-    const uint32_t xfree_peer0 = mapa(smem_u32(&bars[B_X_FREE0]), peer);
-    const int64_t R = (int64_t)a.total_q * H;
-    uint32_t pw = 0, gblk = 0;
-    cluster_wait();  // the peer's barriers are initialised
-
-    // Give this warp's rows of buffer pair g & 1 back: to our own senders
-    // (XO) and to the peer's (our XP is theirs to fill); the pair is free
-    // once all four warps of both CTAs have signalled. The rows' reads are
-    // complete here (their values were consumed before the signal), so the
-    // remote signal needs no release fence.
-    auto release_x = [&](uint32_t g) {
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_X_FREE0 + (g & 1)]);
-        mbar_arrive_remote_relaxed(xfree_peer0 + 8 * (g & 1));
-      }
+    const uint32_t pxfree_peer0 = mapa(smem_u32(&bars[B_PX_FREE0]), peer);
+    const bool arms = warp == (int)(6 - 2 * cta) && lane == 0;  // re-arms PX_FULL
+    uint32_t g = 0;
+    bool dead = false;
+    // the P.V of block x has completed (it read P buffer x & 1)
+    auto wait_pv = [&](uint32_t x) {
+      if (!dead) dead = !mbar_wait<false>(&bars[B_O_DONE0 + (x & 1)], (x >> 1) & 1, abort, limit);
     };
-
+    cluster_wait();
     for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
+      const Item it = decode_item(plan, ord, obase, a.batch, id);
+      float m_prev = -INFINITY, l0 = 0.f, l1 = 0.f;
+      for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
+        const uint32_t b = g & 1, ph = (g >> 1) & 1;
+        if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FULL0 + b], ph, abort, limit);
+        TC_TRACE(arms, TR_RECEIVER, g, 0);
+        const uint8_t* px = sm + kPX + b * kPXBytes + rp * kPXRow;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int q = 0; q < BN / 8; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(px + 16 * q);
+          pk[4 * q] = u.x; pk[4 * q + 1] = u.y; pk[4 * q + 2] = u.z; pk[4 * q + 3] = u.w;
+        }
+        const uint4 ml = *reinterpret_cast<const uint4*>(px + BN * 2);
+        __syncwarp();
+        if (lane == 0 && !dead && !*abort) {
+          if (arms) mbar_arrive_expect_tx(&bars[B_PX_FULL0 + b], kPXTx);  // block g+2
+          mbar_arrive_remote_relaxed(pxfree_peer0 + 8 * b);
+        }
+        const float m_new = __uint_as_float(ml.x);
+        l0 = __uint_as_float(ml.y);
+        l1 = __uint_as_float(ml.z);
+        // the owner rescales its half of O by exactly this factor: same
+        // inputs to the same instruction
+        const bool resc = blk > 0 && __float_as_uint(m_new) != __float_as_uint(m_prev);
+        const float corr = resc ? ex2_approx(m_prev - m_new) : 1.f;
+        m_prev = m_new;
+        // P buffer g & 1 was last read by the P.V of block g - 2; a rescale
+        // of O also needs the P.V of block g - 1 to be done
+        const bool any_resc = __any_sync(0xffffffffu, resc);
+        if (any_resc) wait_pv(g - 1);
+        else if (blk >= 2) wait_pv(g - 2);
+        TC_TRACE(arms, TR_RECEIVER, g, 1);
+        tc_fence_after();
+        if (any_resc) {
+#pragma unroll 1
+          for (int k = 0; k < 8; ++k) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 32 * k, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(t_o + 32 * k, o);
+          }
+        }
+        {
+          uint32_t p01[16], p2[8];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) p01[c] = pk[c];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) p2[c] = pk[16 + c];
+          tmem_st16(tmem + lane_base + tmem_p_col(g & 1, 0), p01);
+          tmem_st8(tmem + lane_base + tmem_p_col(g & 1, 2), p2);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
+        TC_TRACE(arms, TR_RECEIVER, g, 2);
+      }
+      // epilogue: this CTA's 256 value dims of the row, divided by the
+      // owner's final sum, once the item's last P.V is done
+      wait_pv(g - 1);
+      tc_fence_after();
+      const float l = l0 + l1;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int rows_req = it.n * H;
+      const bool valid = it.row0 + r < rows_req;
+      const int64_t grow = (int64_t)it.q0 * H + it.row0 + r;
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        uint32_t o[32];
+        tmem_ld32(t_o + 32 * k, o);
+        if (!valid) continue;
+        if (it.splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + grow * kDv + 256 * cta + 32 * k);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * v + 2 * e]) * inv,
+                                                              __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + ((int64_t)it.split * R + grow) * kDv +
+                                                  256 * cta + 32 * k);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
+    }
+  } else {
+    // ------------------------------------------------------------ softmax, epilogue (own rows)
+    // Two threads per own row: h = 0 takes columns [0, 24) of every block,
+    // h = 1 columns [24, 48). Block g's peer partials arrive in SX buffer
+    // g & 1; the row's P goes to this CTA's TMEM and to the peer's PX
+    // buffer g & 1.
+    const int h = warp >> 2;
+    const int ro = (q4 - 2 * (int)cta) * 32 + lane;
+    const int r = 64 * (int)cta + ro;
+    const int st_idx = 64 * h + ro;                  // 0..127 over the softmax threads
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t t_o = tmem + lane_base + kTmemO + 128 * h;
+    const uint32_t sxfree_peer0 = mapa(smem_u32(&bars[B_SX_FREE0]), peer);
+    const uint32_t px_peer = mapa(smem_u32(sm + kPX + ro * kPXRow), peer);
+    const uint32_t pxfull_peer0 = mapa(smem_u32(&bars[B_PX_FULL0]), peer);
+    const bool arms = warp == (int)(2 * cta) && lane == 0;   // re-arms SX_FULL
+    const int pair_bar = 1 + (q4 & 1);                       // the row's two threads (64 in all)
+    const float scale2 = a.sm_scale * kLog2e;
+    uint32_t g = 0, qi = 0;
+    bool dead = false;
+    cluster_wait();  // the peer's barriers are initialised
+    // the P.V of block x has completed (it read P buffer x & 1)
+    auto wait_pv = [&](uint32_t x) {
+      if (!dead) dead = !mbar_wait<false>(&bars[B_O_DONE0 + (x & 1)], (x >> 1) & 1, abort, limit);
+    };
+
+    // this row's share of the query's latent dims 0..223 into TMEM for item
+    // `id`: h = 0 writes dims 0..127, h = 1 dims 128..223
+    auto load_q = [&](int id) {
+      const Item it = decode_item(plan, ord, obase, a.batch, id);
+      const int64_t qrow = (int64_t)it.q0 * H + it.row0 + r;
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * kDqk + 256 * cta + 128 * h);
+      const bool in = qrow < q_rows;
+      const int nv = h == 0 ? 16 : 12;
+      uint4 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = in && k < nv ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+      if (!dead) dead = !mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort, limit);
+      ++qi;
+      tc_fence_after();
+      uint32_t w0[32], w1[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        w0[4 * k] = v[k].x; w0[4 * k + 1] = v[k].y; w0[4 * k + 2] = v[k].z; w0[4 * k + 3] = v[k].w;
+        w1[4 * k] = v[8 + k].x; w1[4 * k + 1] = v[8 + k].y;
+        w1[4 * k + 2] = v[8 + k].z; w1[4 * k + 3] = v[8 + k].w;
+      }
+      tmem_st32(tmem + lane_base + kTmemQ + 64 * h, w0);
+      if (h == 0) {
+        tmem_st32(tmem + lane_base + kTmemQ + 32, w1);
+      } else {
+        uint32_t w16[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w16[k] = w1[k];
+        tmem_st16(tmem + lane_base + kTmemQ + 96, w16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[B_QT_FULL]);
+    };
+
+    int id = item_of(0, cluster_id, p.nclusters);
+    if (id < total_items) load_q(id);
+    for (int rnd = 0; id < total_items; id = item_of(++rnd, cluster_id, p.nclusters)) {
       const Item it = decode_item(plan, ord, obase, a.batch, id);
       const int rows_req = it.n * H;
       const int row = it.row0 + r;
       const bool valid = row < rows_req;
-      const int i_lo = it.row0 / H;
-      const int i_hi = min(it.n - 1, (it.row0 + BM - 1) / H);
-      const int cnt = i_hi - i_lo + 1;
       const int node = (valid ? row : rows_req - 1) / H;
-      // Mask bytes of a block arrive as (draft node, 8-column group) pairs;
-      // thread r owns pairs r + 128 k. When a tile touches few enough nodes
-      // (every case with 8 or more heads), the bytes of block blk+1 are
-      // loaded while block blk is processed.
       const int pre = kSkip ? it.L - it.n : 0;  // prefix columns: visible, mask unread
+      // Byte mask: the bits of a block arrive as (draft node, 8-column
+      // group) pairs over the nodes of the own rows; softmax thread st_idx
+      // owns pairs st_idx + 128 k. When the own rows touch few enough nodes
+      // (every case with 4 or more heads), the bytes of block blk+1 are
+      // loaded while block blk is processed.
+      const int own0 = min(it.row0 + 64 * (int)cta, rows_req - 1);
+      const int i_lo = own0 / H;
+      const int i_hi = min(it.n - 1, (it.row0 + 64 * (int)cta + kOwnRows - 1) / H);
+      const int cnt = max(1, i_hi - i_lo + 1);
       constexpr int kGroups = BN / 8;  // 8-column groups per block row
       const int pairs = cnt * kGroups;
       const bool prefetch = pairs <= 128 * kMaskPrefetch;
@@ -714,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jb_ = it.j0 + blk_ * BN;
 #pragma unroll
         for (int k = 0; k < kMaskPrefetch; ++k) {
-          const int q = r + 128 * k;
+          const int q = st_idx + 128 * k;
           if (q < pairs) {
             const int pos0 = jb_ + 8 * (q % kGroups);
             const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
@@ -737,18 +982,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (kBits) load_bits(0);
       else if (prefetch) load_mask(0);
-      float m = -INFINITY, l = 0.f;
-      // kWarm: the first item starts with a dry pass (blk = -1) over the
-      // block body while the first scores are still in flight, only to pull
-      // the body's instructions into the SM's caches ahead of the real first
-      // block. It waits on and signals B_DRY (its wait parity, from a
-      // counter one below the first block's, is that of a phase counted as
-      // complete), releases nothing, and its P store lands in columns no
-      // MMA reads yet.
-      const int warm = (kWarm && rnd == 0) ? 1 : 0;
-      gblk -= warm;
-      for (int blk = -warm; blk < it.nblocks; ++blk, ++gblk) {
-        const bool dry = kWarm && blk < 0;
+      float m = -INFINITY, lh = 0.f;
+      for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
+        const uint32_t b = g & 1, ph = (g >> 1) & 1;
         const int jb = it.j0 + blk * BN;
         uint64_t vm;
         if (kBits) {
@@ -760,73 +996,103 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lim = it.j1 - jb;  // columns of this block inside the split
           if (lim < 64) vm &= (1ull << lim) - 1ull;
         } else {
-        // visibility bits of this block for the tile's draft nodes
-        uint8_t* vb = reinterpret_cast<uint8_t*>(vis + (gblk & 1) * kVisNodes);
-        if (prefetch) {
+          // visibility bits of this block for the own rows' draft nodes
+          uint8_t* vb = reinterpret_cast<uint8_t*>(vis + b * kVisNodes);
+          if (prefetch) {
 #pragma unroll
-          for (int k = 0; k < kMaskPrefetch; ++k) {
-            const int q = r + 128 * k;
-            if (q < pairs) {
+            for (int k = 0; k < kMaskPrefetch; ++k) {
+              const int q = st_idx + 128 * k;
+              if (q < pairs) {
+                uint32_t bits = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
+                vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
+              }
+            }
+            if (blk + 1 < it.nblocks) load_mask(blk + 1);
+          } else {
+            for (int q = st_idx; q < pairs; q += 128) {
+              const int pos0 = jb + 8 * (q % kGroups);
+              const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
               uint32_t bits = 0;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
+              for (int e = 0; e < 8; ++e)
+                if (pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) && __ldg(src + e)) bits |= 1u << e;
               vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
             }
           }
-          if (blk + 1 < it.nblocks) load_mask(blk + 1);
-        } else {
-          for (int q = r; q < pairs; q += 128) {
-            const int pos0 = jb + 8 * (q % kGroups);
-            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
-            uint32_t bits = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) && __ldg(src + e)) bits |= 1u << e;
-            vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
-          }
-        }
-        named_bar_sync(1, 128);
-        vm = vis[(gblk & 1) * kVisNodes + (node - i_lo)];
+          named_bar_sync(3, 128);
+          const int ni = node - i_lo;
+          vm = (ni >= 0 && ni < cnt) ? vis[b * kVisNodes + ni] : 0ull;
         }
         if (kSkip && pre > jb) {  // the block's prefix columns, up to the split's end
           const int pc = min(pre, it.j1) - jb;
           vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
         }
+        const uint32_t vh = (uint32_t)(vm >> (kHalfCols * h)) & ((1u << kHalfCols) - 1u);
 
-        // full scores (log2 domain): our fp16 partial plus the peer's
-        const uint32_t xb = gblk & 1;
-        mbar_wait<true>(&bars[dry ? B_DRY : B_X_FULL0 + xb], (gblk >> 1) & 1, abort);
-        const uint8_t* xo = sm + kX + 2 * xb * kXBytes + r * kXRow;
-        const uint8_t* xp = xo + kXBytes;
-        float s[BN];
+        // this CTA's partial scores of the row's 24 columns, from TMEM
+        if (!dead) dead = !mbar_wait<false>(&bars[B_S_FULL0 + b], ph, abort, limit);
+        TC_TRACE(arms, TR_SOFTMAX, g, 0);
+        tc_fence_after();
+        // naturally aligned pieces: columns [0, 16) + [16, 24) for h = 0,
+        // [24, 32) + [32, 48) for h = 1
+        uint32_t own[kHalfCols];
+        {
+          const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b;
+          uint32_t a16[16], a8[8];
+          if (h == 0) {
+            tmem_ld16(tsrc, a16);
+            tmem_ld8(tsrc + 16, a8);
 #pragma unroll
-        for (int q = 0; q < BN / 8; ++q) {
-          const uint4 u = *reinterpret_cast<const uint4*>(xo + 16 * q);
-          const uint4 v = *reinterpret_cast<const uint4*>(xp + 16 * q);
-          const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, vv[4] = {v.x, v.y, v.z, v.w};
+            for (int c = 0; c < 16; ++c) own[c] = a16[c];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fu = __half22float2(*reinterpret_cast<const __half2*>(&uu[e]));
-            const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&vv[e]));
-            s[8 * q + 2 * e] = fu.x + fv.x;
-            s[8 * q + 2 * e + 1] = fu.y + fv.y;
+            for (int c = 0; c < 8; ++c) own[16 + c] = a8[c];
+          } else {
+            tmem_ld8(tsrc + 24, a8);
+            tmem_ld16(tsrc + 32, a16);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) own[c] = a8[c];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) own[8 + c] = a16[c];
           }
         }
-        // the last block's pair stays ours: the epilogue stages rows in it
-        if (kWarm ? (unsigned)blk < (unsigned)(it.nblocks - 1) : blk + 1 < it.nblocks) release_x(gblk);
-
-        // masked online softmax (log2 domain)
-        const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
-        float mx[8];  // eight independent running maxima, then a tree
+        tc_fence_before();
+        mbar_arrive(&bars[B_S_EMPTY0 + b]);
+        // the peer's partials of the same columns (already in the log2 domain)
+        if (!dead) dead = !mbar_wait<true>(&bars[B_SX_FULL0 + b], ph, abort, limit);
+        TC_TRACE(arms, TR_SOFTMAX, g, 1);
+        const uint8_t* sx = sm + kSX + b * kSXBytes + ro * kSXRow + 4 * kHalfCols * h;
+        float s[kHalfCols];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
-          const float v = bit ? s[c] : -INFINITY;
-          s[c] = v;
-          mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
+        for (int q = 0; q < kHalfCols / 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(sx + 16 * q);
+          const float pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * q + e;
+            s[c] = fmaf(__uint_as_float(own[c]), scale2, pv[e]);
+          }
         }
-        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        __syncwarp();
+        if (lane == 0 && !dead && !*abort) {
+          if (arms) mbar_arrive_expect_tx(&bars[B_SX_FULL0 + b], kSXTx);  // block g+2
+          mbar_arrive_remote_relaxed(sxfree_peer0 + 8 * b);
+        }
+
+        // masked maximum of the half row, then of the row
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kHalfCols; ++c) {
+          const float v = (vh >> c) & 1u ? s[c] : -INFINITY;
+          s[c] = v;
+          mx4[c & 3] = fmaxf(mx4[c & 3], v);
+        }
+        const float mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        mxs[(b * kOwnRows + ro) * 2 + h] = mxh;
+        named_bar_sync(pair_bar, 64);
+        TC_TRACE(arms, TR_SOFTMAX, g, 2);
+        const float mb = fmaxf(mxh, mxs[(b * kOwnRows + ro) * 2 + (h ^ 1)]);
         float corr = 1.f;
         bool resc = false;
         if (mb > m + kRescale) {
@@ -835,13 +1101,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[BN / 2];
+        uint32_t pk[kHalfCols / 2];
         if (m == -INFINITY) {
 #pragma unroll
-          for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
+          for (int c = 0; c < kHalfCols / 2; ++c) pk[c] = 0u;
         } else {
 #pragma unroll
-          for (int c = 0; c < BN / 2; ++c) {
+          for (int c = 0; c < kHalfCols / 2; ++c) {
             const float p0 = ex2_approx(s[2 * c] - m), p1 = ex2_approx(s[2 * c + 1] - m);
             const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
             // the denominator sums the same bf16 weights the P.V product uses,
@@ -850,19 +1116,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c] = *reinterpret_cast<const uint32_t*>(&v);
           }
         }
-        l = l * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+        lh = lh * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
 
-        // the previous P.V is done: P and O may be touched
-        if (blk > 0) {
-          mbar_wait<false>(&bars[B_O_DONE], pw & 1, abort);
-          ++pw;
-          tc_fence_after();
+        // the row's half of P, the running max and this half's sum to the
+        // peer, once its receivers have taken block g-2 from that buffer
+        if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FREE0 + b], ph ^ 1, abort, limit);
+        if (!dead && !*abort) {
+          const uint32_t dst = px_peer + b * kPXBytes;
+          const uint32_t bar = pxfull_peer0 + 8 * b;
+#pragma unroll
+          for (int q = 0; q < kHalfCols / 8; ++q)
+            st_async_v4(dst + 48 * h + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
+          if (h == 0) st_async_v2(dst + BN * 2, __float_as_uint(m), __float_as_uint(lh), bar);
+          else st_async_b32(dst + BN * 2 + 8, __float_as_uint(lh), bar);
         }
+        TC_TRACE(arms, TR_SOFTMAX, g, 3);
+
+        // P buffer g & 1 was last read by the P.V of block g - 2; a rescale
+        // of O also needs the P.V of block g - 1 to be done
         const bool need = resc && blk > 0;
-        if (__any_sync(0xffffffffu, need)) {
+        const bool any_need = __any_sync(0xffffffffu, need);
+        if (any_need) wait_pv(g - 1);
+        else if (blk >= 2) wait_pv(g - 2);
+        TC_TRACE(arms, TR_SOFTMAX, g, 4);
+        tc_fence_after();
+        if (any_need) {
           const float f = need ? corr : 1.f;
 #pragma unroll 1
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             uint32_t o[32];
             tmem_ld32(t_o + 32 * k, o);
 #pragma unroll
@@ -870,110 +1151,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(t_o + 32 * k, o);
           }
         }
-        {  // row r of P: 48 bf16 weights as 24 packed columns, in two pieces
-          uint32_t p01[16], p2[8];
+        if (h == 0) {  // keys 0-15 -> piece 0, keys 16-23 -> first half of piece 1
+          uint32_t x8[8], x4[4];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) p01[c] = pk[c];
+          for (int c = 0; c < 8; ++c) x8[c] = pk[c];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) p2[c] = pk[16 + c];
-          tmem_st16(tmem + lane_base + tmem_p_col(0), p01);
-          tmem_st8(tmem + lane_base + tmem_p_col(2), p2);
+          for (int c = 0; c < 4; ++c) x4[c] = pk[8 + c];
+          tmem_st8(tmem + lane_base + tmem_p_col(g & 1, 0), x8);
+          tmem_st4(tmem + lane_base + tmem_p_col(g & 1, 1), x4);
+        } else {       // keys 24-31 -> second half of piece 1, keys 32-47 -> piece 2
+          uint32_t x4[4], x8[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) x4[c] = pk[c];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) x8[c] = pk[4 + c];
+          tmem_st4(tmem + lane_base + tmem_p_col(g & 1, 1) + 4, x4);
+          tmem_st8(tmem + lane_base + tmem_p_col(g & 1, 2), x8);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[dry ? B_DRY : B_P_FULL]);
-        if (dry) {
-          m = -INFINITY;
-          l = 0.f;
-        }
+        mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
+        TC_TRACE(arms, TR_SOFTMAX, g, 5);
       }
-      const uint32_t glast = gblk - 1;
 
-      // epilogue: O / l for this CTA's 256 value dims. Each 128-byte piece of
-      // every row goes through the last block's exchange buffer (still held),
-      // so a warp stores four whole 128-byte row pieces per instruction
-      // instead of 32 scattered 16-byte pieces.
-      mbar_wait<false>(&bars[B_O_DONE], pw & 1, abort);
-      ++pw;
+      // the next item's query (QK may start on it while this epilogue runs)
+      const int next = item_of(rnd + 1, cluster_id, p.nclusters);
+      if (next < total_items) load_q(next);
+
+      // epilogue: O / l for the row's 128 dims of this CTA's half, and the LSE
+      lxs[ro * 2 + h] = lh;
+      named_bar_sync(pair_bar, 64);
+      const float l = lxs[ro * 2] + lxs[ro * 2 + 1];
+      wait_pv(g - 1);  // the item's last P.V
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t row_base = (int64_t)it.q0 * H + it.row0;
-      const int valid_rows = min(BM, rows_req - it.row0);
-      uint8_t* stage = sm + kX + 2 * (glast & 1) * kXBytes;
-      named_bar_sync(3, 128);  // every row has read the last block's scores
-      if (it.splits == 1) {
+      const int64_t grow = (int64_t)it.q0 * H + row;
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {  // 64 bf16 columns per round
-          uint32_t o0[32], o1[32];
-          tmem_ld32(t_o + 64 * k, o0);
-          tmem_ld32(t_o + 64 * k + 32, o1);
-          uint32_t w[32];
+      for (int k = 0; k < 4; ++k) {
+        uint32_t o[32];
+        tmem_ld32(t_o + 32 * k, o);
+        if (!valid) continue;
+        const int col = 256 * (int)cta + 128 * h + 32 * k;
+        if (it.splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + grow * kDv + col);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(o0[2 * e]) * inv,
-                                                            __uint_as_float(o0[2 * e + 1]) * inv);
-            const __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(o1[2 * e]) * inv,
-                                                            __uint_as_float(o1[2 * e + 1]) * inv);
-            w[e] = *reinterpret_cast<const uint32_t*>(&v0);
-            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v1);
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * v + 2 * e]) * inv,
+                                                              __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + ((int64_t)it.split * R + grow) * kDv + col);
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) =
-                make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-          named_bar_sync(3, 128);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int idx = i * 128 + r, rl = idx >> 3, g = idx & 7;
-            if (rl < valid_rows)
-              *reinterpret_cast<uint4*>(a.out + (row_base + rl) * kDv + 256 * cta + 64 * k + 8 * g) =
-                  *reinterpret_cast<const uint4*>(stage + rl * 128 + ((g ^ (rl & 7)) << 4));
-          }
-          named_bar_sync(3, 128);
-        }
-      } else {
-        // split partials in fp16 (each is a convex combination of value rows;
-        // 11 significand bits keep it far below the bf16 output rounding)
-        __half* wso = reinterpret_cast<__half*>(a.ws_o) + ((int64_t)it.split * R + row_base) * kDv + 256 * cta;
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {  // 64 columns per round
-          uint32_t o0[32], o1[32];
-          tmem_ld32(t_o + 64 * k, o0);
-          tmem_ld32(t_o + 64 * k + 32, o1);
-          uint32_t w[32];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const __half2 v0 = __floats2half2_rn(__uint_as_float(o0[2 * e]) * inv,
-                                                 __uint_as_float(o0[2 * e + 1]) * inv);
-            const __half2 v1 = __floats2half2_rn(__uint_as_float(o1[2 * e]) * inv,
-                                                 __uint_as_float(o1[2 * e + 1]) * inv);
-            w[e] = *reinterpret_cast<const uint32_t*>(&v0);
-            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v1);
-          }
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<uint4*>(stage + r * 128 + ((g ^ (r & 7)) << 4)) =
-                make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-          named_bar_sync(3, 128);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int idx = i * 128 + r, rl = idx >> 3, g = idx & 7;
-            if (rl < valid_rows)
-              *reinterpret_cast<uint4*>(wso + (int64_t)rl * kDv + 64 * k + 8 * g) =
-                  *reinterpret_cast<const uint4*>(stage + rl * 128 + ((g ^ (rl & 7)) << 4));
-          }
-          named_bar_sync(3, 128);
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (valid && cta == 0) {
+      if (valid && h == 0) {
         const float lv = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-        const int64_t grow = row_base + r;
         if (it.splits == 1) a.lse[grow] = lv;
         else a.ws_lse[(int64_t)it.split * R + grow] = lv;
       }
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
-      release_x(glast);  // staging done: the peer may refill this buffer
     }
   }
 
@@ -982,7 +1228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // grid) may start its set-up; it waits for this grid's completion before
   // reading any partial
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (tid == 0 && *abort) flag(a.status, MT_DEV_TIMEOUT);
+  if (tid == 0 && *abort) {
+    flag(a.status, MT_DEV_TIMEOUT);
+    // remote stores issued before the give-up land within microseconds
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < kAbortSettleNs) {
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -998,6 +1250,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::mutex g_dev_mu;
 int g_clusters[64] = {0};
+int g_test_drop_item = -1;
+unsigned long long g_test_limit_ns = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   std::call_once(g_encode_once, [] {
@@ -1027,22 +1281,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols
 
 using KernelFn = void (*)(TcParams, CUtensorMap, CUtensorMap, CUtensorMap);
 
-// The instantiations: byte mask (no dry pass) or bit mask, each with and
-// without the prefix skip.
-constexpr int kVariants = 6;
+// The instantiations: byte or bit mask, each with and without the prefix skip.
+constexpr int kVariants = 4;
 KernelFn kernel_variant(int i) {
   switch (i) {
-    case 0: return verify_tc_kernel<false, false, false>;
-    case 1: return verify_tc_kernel<false, false, true>;
-    case 2: return verify_tc_kernel<true, false, false>;
-    case 3: return verify_tc_kernel<true, false, true>;
-    case 4: return verify_tc_kernel<true, true, false>;
-    default: return verify_tc_kernel<true, true, true>;
+    case 0: return verify_tc_kernel<false, false>;
+    case 1: return verify_tc_kernel<false, true>;
+    case 2: return verify_tc_kernel<true, false>;
+    default: return verify_tc_kernel<true, true>;
   }
 }
-int variant_index(bool bits, bool warm, bool skip) {
-  return !bits ? (skip ? 1 : 0) : (warm ? 4 : 2) + (skip ? 1 : 0);
-}
+int variant_index(bool bits, bool skip) { return (bits ? 2 : 0) + (skip ? 1 : 0); }
 
 // Clusters of two that fit at once on this device (persistent grid size).
 int device_clusters(int num_sms) {
@@ -1074,9 +1323,14 @@ int device_clusters(int num_sms) {
 
 }  // namespace tc
 
+void set_tc_test_hooks(int drop_item, unsigned long long limit_ns) {
+  tc::g_test_drop_item = drop_item;
+  tc::g_test_limit_ns = limit_ns;
+}
+
 cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stream) {
   using namespace tc;
-  if (a.batch > kMaxBatch || a.num_slots <= 0 || a.num_slots >= 0x7fffffffLL ||
+  if (a.num_slots <= 0 || a.num_slots >= 0x7fffffffLL ||
       (long long)a.total_q * a.heads >= 0x7fffffffLL)
     return cudaErrorNotSupported;
   const int nclusters = device_clusters(num_sms > 0 ? num_sms : 148);
@@ -1087,10 +1341,8 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
       !make_map(&tkv_lat, a.kv, (uint64_t)a.num_slots, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&tkv_rope, a.kv, (uint64_t)a.num_slots, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorNotSupported;
-  TcParams p;
-  p.a = a;
-  p.a.partial_f16 = 1;
-  p.nclusters = nclusters;
+  VerifyArgs full = a;
+  full.partial_f16 = 0;  // split partials in fp32
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters);
   cfg.blockDim = dim3(kThreads);
@@ -1107,24 +1359,41 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // The dry passes cost a few instructions in every block and save a few
-  // microseconds of instruction fetch once per CTA: they pay when each
-  // cluster has at most a few hundred key blocks to do. An upper bound from
-  // the host-known sizes (every tile against the whole kv_indices) decides.
-  const long long tiles_ub = ((long long)a.total_q * a.heads + BM - 1) / BM + a.batch;
-  const bool warm = a.bits_mask && tiles_ub * a.kv_len <= (long long)kWarmBlocks * BN * nclusters;
-  const KernelFn fn = kernel_variant(variant_index(a.bits_mask != 0, warm, a.skip_prefix != 0));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p, tq_rope, tkv_lat, tkv_rope);
-  if (e != cudaSuccess) return e;
-  if (a.max_splits > 1) return launch_lse_merge(p.a, stream);
+  const KernelFn fn = kernel_variant(variant_index(a.bits_mask != 0, a.skip_prefix != 0));
+  // The plan of a launch lives in shared memory: requests go in chunks of
+  // kMaxBatch, one launch each, with the indptrs offset to the chunk.
+  for (int b0 = 0; b0 < a.batch; b0 += kMaxBatch) {
+    TcParams p;
+    p.a = full;
+    p.a.batch = min(kMaxBatch, a.batch - b0);
+    p.a.kv_indptr = a.kv_indptr + b0;
+    p.a.qo_indptr = a.qo_indptr + b0;
+    p.a.mask_indptr = a.mask_indptr + b0;
+    p.nclusters = nclusters;
+    p.first_chunk = b0 == 0;
+    p.last_chunk = b0 + kMaxBatch >= a.batch;
+    p.drop_item = g_test_drop_item;
+    p.limit_ns = g_test_limit_ns > 0 ? g_test_limit_ns : sm100::kWaitLimitNs;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p, tq_rope, tkv_lat, tkv_rope);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.max_splits > 1) return launch_lse_merge(full, stream);
   return cudaSuccess;
 }
+
+#ifdef MT_TC_TRACE
+// Copies the pipeline trace of the last traced launch to host memory.
+extern "C" int mla_tree_tc_trace_read(void* host, size_t bytes) {
+  if (bytes < sizeof(tc::g_tc_trace)) return -1;
+  return cudaMemcpyFromSymbol(host, tc::g_tc_trace, sizeof(tc::g_tc_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 int verify_tc_launches(int batch, int total_q, int heads, int max_splits) {
   (void)total_q;
   (void)heads;
-  if (batch > tc::kMaxBatch) return 0;
-  return max_splits > 1 ? 2 : 1;
+  if (batch <= 0) return 0;
+  return (batch + tc::kMaxBatch - 1) / tc::kMaxBatch + (max_splits > 1 ? 1 : 0);
 }
 
 }  // namespace mt

@@ -296,10 +296,11 @@ def stress(w: Workload, kind: str) -> Workload:
     peaked  every query value x8: scaled scores spread over tens of log2
             units, so the softmax is dominated by a few keys per row.
     cancel  key latent dims 256..511 copy dims 0..255; query dims 0..255
-            x16 and dims 256..511 their negation. The latent dot product is
-            exactly zero, but its two halves are large and of opposite sign,
-            so any kernel that rounds per-half partial scores loses the
-            (rope-only) score.
+            x64 and dims 256..511 their negation; query rope dims x4. The
+            latent dot product is exactly zero, but its two halves are
+            large (hundreds of log2 units once scaled) and of opposite
+            sign, so any kernel that rounds per-half partial scores loses
+            the (rope-only, moderately peaked) score.
     huge_v  key latent dims x2^17 and query latent dims x2^-17: the scores
             are those of ``w``, while the values (latent dims) reach
             several times 2^17, beyond the largest finite fp16 number.
@@ -310,8 +311,9 @@ def stress(w: Workload, kind: str) -> Workload:
     if kind == "cancel":
         def qf(q):
             q = q.clone()
-            q[..., :256] *= 16.0
+            q[..., :256] *= 64.0
             q[..., 256:512] = -q[..., :256]
+            q[..., D_LATENT:] *= 4.0
             return q
 
         def rf(r):

@@ -49,8 +49,20 @@ def sample_rows(w, per_request, seed=0):
     return rows
 
 
-def compare_attention(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
-    """Assert the verify tolerances; returns the stats."""
+# bf16 keeps 8 significant bits: rounding the output to the nearest bf16
+# moves it by at most 2^-9 of its magnitude
+BF16_HALF_ULP_REL = 2.0 ** -9
+
+
+def compare_attention(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, rounding_term=False):
+    """Assert the verify tolerances; returns the stats.
+
+    rounding_term: the absolute bounds (max 1e-2, mean 1e-3) hold for
+    outputs below about 2.5 in magnitude, where the final rounding to bf16
+    moves a value by less than 0.005. Inputs that drive single outputs
+    further out (a peaked softmax returns single value entries of size 4-5,
+    where half a bf16 ulp is 0.0156) add that unavoidable rounding, at most
+    2^-9 |ref| per element, to both bounds."""
     o = out_gpu.detach().float().cpu().numpy().astype(np.float64)
     l = lse_gpu.detach().cpu().numpy().astype(np.float64)
     if rows is not None:
@@ -58,6 +70,8 @@ def compare_attention(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
         o, l, out_ref, lse_ref = o[ts, hs], l[ts, hs], out_ref[ts, hs], lse_ref[ts, hs]
     assert np.isfinite(out_ref).all()
     err = np.abs(o - out_ref)
+    if rounding_term:
+        err = np.maximum(err - BF16_HALF_ULP_REL * np.abs(out_ref), 0.0)
     finite = np.isfinite(lse_ref)
     assert (np.isneginf(l[~finite])).all(), "rows with nothing visible must give lse = -inf"
     lerr = np.abs(l[finite] - lse_ref[finite]) / np.maximum(1.0, np.abs(lse_ref[finite]))

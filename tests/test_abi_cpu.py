@@ -175,3 +175,18 @@ def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(abi.MlaTreeError):
         abi._ptr(torch.zeros(4), None, "x")
+
+
+def test_wait_limit_hook_arguments(lib):
+    assert lib.mla_tree_test_wait_limits(-2, 0) == abi.MT_EINVAL
+    assert lib.mla_tree_test_wait_limits(-1, -1) == abi.MT_EINVAL
+    assert lib.mla_tree_test_wait_limits(3, 1000) == abi.MT_OK
+    assert lib.mla_tree_test_wait_limits(-1, 0) == abi.MT_OK
+
+
+def test_launch_count_many_requests(lib):
+    """The tensor-core path takes any number of requests, in launches of at
+    most 256 (plus the merge when splits are possible)."""
+    assert lib.mla_tree_verify_launch_count(256, 256 * 16, 8, 1, 2) == 1
+    assert lib.mla_tree_verify_launch_count(257, 257 * 16, 8, 1, 2) == 2
+    assert lib.mla_tree_verify_launch_count(600, 600 * 16, 8, 4, 2) == 4

@@ -6,7 +6,9 @@ workloads the way a serving engine runs them, against the fp64 oracle.
   fp16 range. Every factor is a power of two, so the inputs are exact in
   bf16 and the oracle's expectations need no other reasoning. Both kernels,
   unsplit and split (the split partials and their merge are where a narrow
-  intermediate format would overflow or round).
+  intermediate format would overflow or round). These inputs push single
+  outputs to magnitudes of 4-5, so the comparison adds the bf16 rounding of
+  the output itself (2^-9 |ref|) to the stated bounds.
 * The 64-request ragged workload (prefixes 128..131072, 8..64-node trees,
   64 heads, 2^22-slot pool), captured once as one CUDA graph of the whole
   step (fused marshaling + verify) and replayed on a second draw of the same
@@ -61,9 +63,9 @@ def test_stress_inputs(kind, path, splits):
         # values are 2^17 times those of a normal draw: compare at that scale
         s = 2.0 ** 17
         assert torch.isfinite(st.out.float()).all()
-        compare_attention(st.out.float() / s, st.lse, out / s, lse)
+        compare_attention(st.out.float() / s, st.lse, out / s, lse, rounding_term=True)
     else:
-        compare_attention(st.out, st.lse, out, lse)
+        compare_attention(st.out, st.lse, out, lse, rounding_term=True)
 
 
 def test_config5_graph_replay_two_draws():

@@ -156,6 +156,30 @@ def test_graph_capture_and_replay(path):
         compare_attention(st.out, st.lse, out, lse)
 
 
+@pytest.mark.parametrize("bits", [False, True], ids=["bytes", "bits"])
+def test_more_requests_than_one_launch_plans(bits):
+    """300 requests of one 128-row tile each: the tensor-core path serves
+    them in launches of at most 256 requests (no fall-back to the other
+    kernel), split and unsplit, and agrees with the oracle on every row.
+    With only 46..316 keys per request some outputs reach magnitudes of 2-4,
+    where rounding the exact result to bf16 alone moves it by up to 0.0078,
+    so the comparison adds that rounding (2^-9 |ref|) to the bounds."""
+    import numpy as np
+    rng = np.random.default_rng(300)
+    prefix = [int(x) for x in rng.integers(30, 300, size=300)]
+    w = W.make_workload("many", 8, prefix, "uniform", [16] * 300, 131072, seed=300)
+    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, 1, abi.PATH_AUTO) == 2
+    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, 4, abi.PATH_TC) == 3
+    ref = _oracle("many", w)
+    out, lse = ref.attention()
+    for splits in (1, 4):
+        st = VerifyStep(w, path=abi.PATH_AUTO, max_splits=splits, mask_bits=bits)
+        st.run()
+        torch.cuda.synchronize()
+        assert int(st.status.item()) == 0
+        compare_attention(st.out, st.lse, out, lse, rounding_term=True)
+
+
 def test_bad_slot_sets_status_and_skips():
     w = W.small(seed=8)
     st = VerifyStep(w, path=abi.PATH_SIMT)

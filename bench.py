@@ -398,7 +398,8 @@ def run_ours(args):
     achieved_tf = flops / (verify_ms * 1e-3) / 1e12
     t_hbm, t_tc = byts / (hbm * 1e9), flops / (tf_burst * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    launches_verify = abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, args.max_splits, args.path)
+    launches_verify = abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, st.kv_indices.numel(),
+                                                       args.max_splits, args.path)
     launches = args.steps * (ncalls - 1 + launches_verify)
 
     # end to end through the public API with host buffers

@@ -197,8 +197,12 @@ size_t mla_tree_verify_workspace_bytes(int batch, int total_q, int heads, int ma
 /*
  * Number of kernels one mla_tree_verify call with these host scalars
  * launches (for launch accounting; 0 for arguments the call would reject).
+ * kv_indices_len is the call's kv_indices_len: the warp-shuffle kernel
+ * needs no merge launch when no request can hold more keys than one of its
+ * splits takes.
  */
-int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_splits, int path);
+int mla_tree_verify_launch_count(int batch, int total_q, int heads, int64_t kv_indices_len,
+                                 int max_splits, int path);
 
 /*
  * Test facility for the kernels' failure detection (the paper has no

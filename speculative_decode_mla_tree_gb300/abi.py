@@ -59,7 +59,7 @@ def load():
     lib.mla_tree_verify_workspace_bytes.restype = SZ
     lib.mla_tree_verify_workspace_bytes.argtypes = [I32, I32, I32, I32]
     lib.mla_tree_verify_launch_count.restype = I32
-    lib.mla_tree_verify_launch_count.argtypes = [I32, I32, I32, I32, I32]
+    lib.mla_tree_verify_launch_count.argtypes = [I32, I32, I32, I64, I32, I32]
     lib.mla_tree_verify.restype = I32
     lib.mla_tree_verify.argtypes = [P, P, I64, P, I64, P, P, P, I64, P, I32, I32, I32, F32,
                                     P, P, P, SZ, I32, I32, P, P]
@@ -194,8 +194,8 @@ def mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits=0):
     return int(load().mla_tree_verify_workspace_bytes(batch, total_q, heads, max_splits))
 
 
-def mla_tree_verify_launch_count(batch, total_q, heads, max_splits=0, path=PATH_AUTO):
-    return int(load().mla_tree_verify_launch_count(batch, total_q, heads, max_splits, path))
+def mla_tree_verify_launch_count(batch, total_q, heads, kv_indices_len, max_splits=0, path=PATH_AUTO):
+    return int(load().mla_tree_verify_launch_count(batch, total_q, heads, kv_indices_len, max_splits, path))
 
 
 def mla_tree_verify(q, kv_buf, kv_indices, kv_indptr, qo_indptr, packed_mask, mask_indptr,

@@ -172,9 +172,10 @@ int mla_tree_test_wait_limits(int drop_item, int64_t wait_limit_ns) {
   return MT_OK;
 }
 
-int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_splits, int path) {
-  if (batch < 0 || total_q < 0 || heads <= 0 || max_splits < 0 || max_splits > MT_MAX_SPLITS ||
-      path < 0 || path > 2)
+int mla_tree_verify_launch_count(int batch, int total_q, int heads, int64_t kv_indices_len,
+                                 int max_splits, int path) {
+  if (batch < 0 || total_q < 0 || heads <= 0 || kv_indices_len < 0 || max_splits < 0 ||
+      max_splits > MT_MAX_SPLITS || path < 0 || path > 2)
     return 0;
   if (batch == 0 || total_q == 0) return 0;
   if (max_splits == 0) max_splits = auto_max_splits(batch, total_q, heads, sm_count());
@@ -184,7 +185,7 @@ int mla_tree_verify_launch_count(int batch, int total_q, int heads, int max_spli
     if (n > 0) return n;
     if (path == 2) return 0;
   }
-  return max_splits > 1 ? 2 : 1;
+  return simt_may_split(max_splits, kv_indices_len) ? 2 : 1;
 }
 
 }  // extern "C"
@@ -238,7 +239,6 @@ static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
   a.out = out;
   a.lse = lse;
   a.max_splits = max_splits;
-  a.partial_f16 = 0;
   a.status = dev_status;
   char* ws = (char*)workspace;
   a.ws_tok = (int32_t*)(ws + wl.tok_off);
@@ -261,7 +261,7 @@ static int verify_common(const mt_bf16* q, const mt_bf16* kv_buf, int64_t num_sl
   }
   cudaError_t e = launch_verify_simt(a, nsm, s);
   if (e != cudaSuccess) return MT_ECUDA;
-  if (max_splits > 1) e = launch_lse_merge(a, s);
+  if (simt_may_split(max_splits, kv_indices_len)) e = launch_lse_merge(a, s);
   return cuda_status(e);
 }
 

@@ -27,7 +27,6 @@ struct VerifyArgs {
   uint16_t* out;                // bf16 [total_q, heads, 512]
   float* lse;                   // fp32 [total_q, heads]
   int max_splits;               // capacity of the partial buffers
-  int partial_f16;              // split partials stored as fp16 (else fp32; the merge reads either)
   int32_t* status;
   // workspace views
   int32_t* ws_tok;              // [total_q] split count of each token's request (0: not
@@ -70,6 +69,8 @@ cudaError_t launch_prepare(const uint16_t* src, int64_t src_stride, const int32_
                            int64_t word_capacity, int32_t* status, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream);
+// Whether a warp-shuffle call may split a request, i.e. needs the merge.
+bool simt_may_split(int max_splits, int64_t kv_len);
 cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream);
 // Tensor-core path; returns cudaErrorNotSupported when it cannot serve `a`.
 cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stream);

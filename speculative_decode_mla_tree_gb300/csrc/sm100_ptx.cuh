@@ -197,6 +197,34 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same two with the accumulate flag fixed at compile time (no
+// predicate to compute per instruction).
+template <int kAcc>
+__device__ __forceinline__ void mma_bf16_ss_c(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+template <int kAcc>
+__device__ __forceinline__ void mma_bf16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+
+// A shared-memory descriptor moved by `bytes` (a multiple of 16): the start
+// address is the low 14-bit field in 16-byte units, and shared-memory
+// addresses stay below 256 KB, so the add never carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

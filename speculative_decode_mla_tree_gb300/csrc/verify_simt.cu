@@ -6,29 +6,35 @@
 // log-sum-exp merge, after "Flipping the Switch", section "The Broader
 // Context".
 //
-// One warp owns one draft token and up to kRows heads of it, for one KV
-// split. Lane l holds latent dims [16 l, 16 l + 16) and rope dims
-// [512 + 2 l, 512 + 2 l + 2) of the query rows, so one pool row is read
-// with two 16-byte loads and one 4-byte load per lane (1152 contiguous bytes
-// per warp) and serves both the score (all 576 dims) and the value update
-// (the 512 latent dims the lane already holds). Scores are reduced with xor
+// One CTA of kWarps warps owns one draft token, up to kRows heads of it and
+// one KV split. The warps cut the split's key range into kWarps contiguous
+// pieces and run an online softmax over their piece; the pieces are merged
+// in shared memory at the end, so a request of up to kMinKeysY keys needs
+// no split and no merge launch. Lane l holds latent dims [16 l, 16 l + 16)
+// and rope dims [512 + 2 l, 512 + 2 l + 2) of the query rows, so one pool
+// row is read with two 16-byte loads and one 4-byte load per lane (1152
+// contiguous bytes per warp) and serves both the score (all 576 dims) and
+// the value update (the 512 latent dims the lane already holds). Keys go
+// two at a time, so their row loads overlap. Scores are reduced with xor
 // shuffles, so every lane holds the same bits; the online softmax runs in
 // the log2 domain with sm_scale * log2(e) folded into q.
-#include <cuda_fp16.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "mt_common.cuh"
 #include "mt_internal.h"
 
 namespace mt {
 
-constexpr int kRows = 4;          // heads per warp
-constexpr int kWarps = 4;         // warps per CTA
-constexpr int kMinChunk = 8;      // smallest KV split worth a warp (keys are a serial latency chain)
+constexpr int kRows = 4;          // heads per CTA
+constexpr int kWarps = 8;         // warps per CTA, splitting its key range
+constexpr int kMinKeysY = 256;    // smallest KV split of the grid (keys)
+constexpr int kSimtSmem = kWarps * kRows * kDv * 4;  // the warps' partial outputs
 
 __device__ __forceinline__ int simt_splits(int L, int max_splits, int* chunk) {
   int c = (L + max_splits - 1) / max_splits;
-  if (c < kMinChunk) c = kMinChunk;
+  if (c < kMinKeysY) c = kMinKeysY;
   *chunk = c;
   const int s = (L + c - 1) / c;
   return s < 1 ? 1 : s;
@@ -52,18 +58,19 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   // launched as a programmatic dependent of the previous kernel in the
   // stream: wait for it to complete before reading anything it may write
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  extern __shared__ float part_o[];             // [kWarps][kRows][512]
+  __shared__ float part_m[kWarps][kRows], part_l[kWarps][kRows];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int hg_count = (a.heads + kRows - 1) / kRows;
-  const int64_t t = wid / hg_count;
-  const int h0 = (int)(wid - t * hg_count) * kRows;
+  const int64_t t = blockIdx.x / hg_count;
+  const int h0 = (int)(blockIdx.x - t * hg_count) * kRows;
   if (t >= a.total_q) return;
   const int split = blockIdx.y;
   const int b = find_request(a.qo_indptr, a.batch, t);
   const ReqGeom g = request_geom(a.kv_indptr, a.qo_indptr, a.mask_indptr, b, a.kv_len,
                                  a.mask_len, a.total_q, a.bits_mask != 0);
   if (!g.ok || t < g.q0 || t >= g.q0 + g.n) {
-    if (lane == 0 && split == 0) {
+    if (tid == 0 && split == 0) {
       flag(a.status, MT_DEV_BAD_INDPTR);
       if (h0 == 0) a.ws_tok[t] = 0;  // nothing to merge for this token
     }
@@ -71,10 +78,12 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   }
   int chunk;
   const int S = simt_splits(g.L, a.max_splits, &chunk);
-  if (split == 0 && lane == 0 && h0 == 0) a.ws_tok[t] = S;
+  if (split == 0 && tid == 0 && h0 == 0) a.ws_tok[t] = S;
   if (split >= S) return;
   const int j0 = split * chunk;
   const int j1 = min(g.L, j0 + chunk);
+  const int per = (j1 - j0 + kWarps - 1) / kWarps;  // this warp's piece
+  const int wj0 = min(j1, j0 + w * per), wj1 = min(j1, wj0 + per);
 
   const float qscale = a.sm_scale * kLog2e;
   float qv[kRows][18];
@@ -102,78 +111,124 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
   const int64_t mrow0 = g.mask0 + (t - g.q0) * (int64_t)g.mask_row;
   const int32_t* idx = a.kv_indices + g.kv0;
   const int pre = a.skip_prefix ? g.L - g.n : 0;  // columns visible without a mask read
-  for (int j = j0; j < j1; ++j) {
-    const int32_t slot = __ldg(idx + j);
-    if (slot < 0 || slot >= a.num_slots) {
-      if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
-      continue;
+  auto visible = [&](int j) -> bool {
+    return j < pre ? true
+           : a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u) != 0
+                         : __ldg(a.mask + mrow0 + j) != 0;
+  };
+  auto usable = [&](int32_t slot) -> bool {
+    if (slot >= 0 && slot < a.num_slots) return true;
+    if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
+    return false;
+  };
+  // one key of row r: its score and the online-softmax update
+  auto update = [&](int r, const float (&kf)[18]) {
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < 18; ++e) d = fmaf(qv[r][e], kf[e], d);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (d > m[r]) {
+      const float c = exp2f(m[r] - d);
+      l[r] *= c;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[r][e] *= c;
+      m[r] = d;
     }
-    const bool vis = j < pre ? true
-                     : a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u)
-                                   : __ldg(a.mask + mrow0 + j) != 0;
-    if (!vis) continue;
-    float kf[18];
-    load_row18(a.kv + (int64_t)slot * kDqk, lane, 1.f, kf);
+    const float p = exp2f(d - m[r]);
+    l[r] += p;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[r][e] = fmaf(p, kf[e], acc[r][e]);
+  };
+  for (int j = wj0; j < wj1; j += 2) {
+    const bool two = j + 1 < wj1;
+    const int32_t s0 = __ldg(idx + j), s1 = two ? __ldg(idx + j + 1) : 0;
+    const bool v0 = usable(s0) && visible(j);
+    const bool v1 = two && usable(s1) && visible(j + 1);
+    float k0[18], k1[18];
+    if (v0) load_row18(a.kv + (int64_t)s0 * kDqk, lane, 1.f, k0);
+    if (v1) load_row18(a.kv + (int64_t)s1 * kDqk, lane, 1.f, k1);
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-      float d = 0.f;
-#pragma unroll
-      for (int e = 0; e < 18; ++e) d = fmaf(qv[r][e], kf[e], d);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if (d > m[r]) {
-        const float c = exp2f(m[r] - d);
-        l[r] *= c;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[r][e] *= c;
-        m[r] = d;
-      }
-      const float p = exp2f(d - m[r]);
-      l[r] += p;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[r][e] = fmaf(p, kf[e], acc[r][e]);
+      if (v0) update(r, k0);
+      if (v1) update(r, k1);
     }
   }
 
-  const int64_t R = (int64_t)a.total_q * a.heads;
+  // merge the warps' pieces
 #pragma unroll
   for (int r = 0; r < kRows; ++r) {
-    const int h = h0 + r;
-    if (h >= a.heads) continue;
-    const int64_t row = t * a.heads + h;
-    const bool any = l[r] > 0.f;
-    const float inv = any ? 1.f / l[r] : 0.f;
-    const float row_lse = any ? (m[r] + log2f(l[r])) * kLn2 : -INFINITY;
-    if (S == 1) {
-      uint32_t w[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[r][2 * e] * inv, acc[r][2 * e + 1] * inv);
-        w[e] = *reinterpret_cast<const uint32_t*>(&v);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv) + 2 * lane;
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      if (lane == 0) a.lse[row] = row_lse;
-    } else {
-      float4* dst = reinterpret_cast<float4*>(a.ws_o + ((int64_t)split * R + row) * kDv) + 4 * lane;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dst[e] = make_float4(acc[r][4 * e] * inv, acc[r][4 * e + 1] * inv, acc[r][4 * e + 2] * inv,
-                             acc[r][4 * e + 3] * inv);
-      if (lane == 0) a.ws_lse[(int64_t)split * R + row] = row_lse;
+    if (lane == 0) {
+      part_m[w][r] = m[r];
+      part_l[w][r] = l[r];
     }
+    float4* dst = reinterpret_cast<float4*>(part_o + (w * kRows + r) * kDv + 16 * lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      dst[e] = make_float4(acc[r][4 * e], acc[r][4 * e + 1], acc[r][4 * e + 2], acc[r][4 * e + 3]);
+  }
+  __syncthreads();
+  const int r = tid >> 6, d0 = (tid & 63) * 8;  // this thread's head and 8 dims
+  const int h = h0 + r;
+  if (h >= a.heads) return;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) mx = fmaxf(mx, part_m[k][r]);
+  float tot = 0.f, o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) {
+      const float mk = part_m[k][r];
+      if (mk == -INFINITY) continue;
+      const float c = exp2f(mk - mx);
+      tot = fmaf(c, part_l[k][r], tot);
+      const float4* src = reinterpret_cast<const float4*>(part_o + (k * kRows + r) * kDv + d0);
+      const float4 x0 = src[0], x1 = src[1];
+      o[0] = fmaf(c, x0.x, o[0]); o[1] = fmaf(c, x0.y, o[1]);
+      o[2] = fmaf(c, x0.z, o[2]); o[3] = fmaf(c, x0.w, o[3]);
+      o[4] = fmaf(c, x1.x, o[4]); o[5] = fmaf(c, x1.y, o[5]);
+      o[6] = fmaf(c, x1.z, o[6]); o[7] = fmaf(c, x1.w, o[7]);
+    }
+  }
+  const int64_t R = (int64_t)a.total_q * a.heads;
+  const int64_t row = t * a.heads + h;
+  const bool any = tot > 0.f;
+  const float inv = any ? 1.f / tot : 0.f;
+  const float row_lse = any ? (mx + log2f(tot)) * kLn2 : -INFINITY;
+  if (S == 1) {
+    uint32_t wv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
+      wv[e] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(a.out + row * kDv + d0) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    if (d0 == 0) a.lse[row] = row_lse;
+  } else {
+    float4* dst = reinterpret_cast<float4*>(a.ws_o + ((int64_t)split * R + row) * kDv + d0);
+    dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+    dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+    if (d0 == 0) a.ws_lse[(int64_t)split * R + row] = row_lse;
   }
 }
 
+static std::once_flag g_simt_attr_once;
+static cudaError_t g_simt_attr = cudaSuccess;
+
 cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t stream) {
   (void)num_sms;
+  std::call_once(g_simt_attr_once, [] {
+    g_simt_attr = cudaFuncSetAttribute(verify_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSimtSmem);
+  });
+  if (g_simt_attr != cudaSuccess) return g_simt_attr;
   const int hg_count = (a.heads + kRows - 1) / kRows;
-  const int64_t warps = (int64_t)a.total_q * hg_count;
-  const int64_t blocks = (warps + kWarps - 1) / kWarps;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks, (unsigned)a.max_splits);
+  cfg.gridDim = dim3((unsigned)((int64_t)a.total_q * hg_count), (unsigned)a.max_splits);
   cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = kSimtSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -183,12 +238,16 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, verify_simt_kernel, a);
 }
 
+// Whether a warp-shuffle call with these host-known sizes may split a
+// request (and so needs the merge): only when some request can have more
+// keys than one split of the grid takes.
+bool simt_may_split(int max_splits, int64_t kv_len) { return max_splits > 1 && kv_len > kMinKeysY; }
+
 // ---------------------------------------------------------------- merge
 
 // lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s  -> bf16.
-// One CTA per (token, group of heads). Each thread owns the 16 bytes of a
-// partial row that one vector load brings in: 8 dims of an fp16 partial
-// (tensor-core path) or 4 of an fp32 one (warp-shuffle path). The producing
+// One CTA per (token, group of heads). Each thread owns the 16 bytes of an
+// fp32 partial row that one vector load brings in (4 dims). The producing
 // kernel records each token's split count, so one load decides the work.
 // Then the LSEs and partials of up to kMergeGroup splits are loaded at once:
 // two dependent memory rounds per row. More splits are taken in further
@@ -209,15 +268,6 @@ __device__ __forceinline__ void unpack16(const uint4 u, const float*, float (&x)
   x[1] = __uint_as_float(u.y);
   x[2] = __uint_as_float(u.z);
   x[3] = __uint_as_float(u.w);
-}
-__device__ __forceinline__ void unpack16(const uint4 u, const __half*, float (&x)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-    x[2 * e] = f.x;
-    x[2 * e + 1] = f.y;
-  }
 }
 
 template <typename P>
@@ -287,11 +337,8 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const VerifyAr
     const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
     o[e] = *reinterpret_cast<const uint32_t*>(&b);
   }
-  uint16_t* dst = a.out + row * kDv + kVec * dv;
-  if (kVec == 8)
-    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2 % (kVec / 2)], o[3 % (kVec / 2)]);  // kVec / 2 == 4 here
-  else
-    *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+  static_assert(kVec == 4, "fp32 partials: 4 dims per 16-byte load");
+  *reinterpret_cast<uint2*>(a.out + row * kDv + kVec * dv) = make_uint2(o[0], o[1]);
   if (dv == 0) a.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
@@ -300,7 +347,7 @@ cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
   // producing kernel drains and waits on-device for its completion, which
   // hides the launch gap between the two.
   cudaLaunchConfig_t cfg = {};
-  const int heads_per_cta = a.partial_f16 ? MergeShape<__half>::kHeads : MergeShape<float>::kHeads;
+  const int heads_per_cta = MergeShape<float>::kHeads;
   cfg.gridDim = dim3((unsigned)a.total_q, (unsigned)((a.heads + heads_per_cta - 1) / heads_per_cta));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = stream;
@@ -309,7 +356,6 @@ cudaError_t launch_lse_merge(const VerifyArgs& a, cudaStream_t stream) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (a.partial_f16) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__half>, a);
   return cudaLaunchKernelEx(&cfg, lse_merge_kernel<float>, a);
 }
 

@@ -1342,7 +1342,6 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, int num_sms, cudaStream_t stre
       !make_map(&tkv_rope, a.kv, (uint64_t)a.num_slots, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorNotSupported;
   VerifyArgs full = a;
-  full.partial_f16 = 0;  // split partials in fp32
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters);
   cfg.blockDim = dim3(kThreads);

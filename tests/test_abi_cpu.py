@@ -187,6 +187,15 @@ def test_wait_limit_hook_arguments(lib):
 def test_launch_count_many_requests(lib):
     """The tensor-core path takes any number of requests, in launches of at
     most 256 (plus the merge when splits are possible)."""
-    assert lib.mla_tree_verify_launch_count(256, 256 * 16, 8, 1, 2) == 1
-    assert lib.mla_tree_verify_launch_count(257, 257 * 16, 8, 1, 2) == 2
-    assert lib.mla_tree_verify_launch_count(600, 600 * 16, 8, 4, 2) == 4
+    assert lib.mla_tree_verify_launch_count(256, 256 * 16, 8, 100000, 1, 2) == 1
+    assert lib.mla_tree_verify_launch_count(257, 257 * 16, 8, 100000, 1, 2) == 2
+    assert lib.mla_tree_verify_launch_count(600, 600 * 16, 8, 100000, 4, 2) == 4
+
+
+def test_launch_count_short_rows_need_no_merge(lib):
+    """The warp-shuffle kernel splits a request across the grid only beyond
+    256 keys: a call whose kv_indices are no longer launches one kernel."""
+    assert lib.mla_tree_verify_launch_count(1, 9, 8, 30, 0, 0) == 1      # the live 9-node shape
+    assert lib.mla_tree_verify_launch_count(1, 9, 8, 30, 64, 1) == 1
+    assert lib.mla_tree_verify_launch_count(1, 9, 8, 5000, 64, 1) == 2
+    assert lib.mla_tree_verify_launch_count(1, 9, 8, 5000, 1, 1) == 1

@@ -168,8 +168,9 @@ def test_more_requests_than_one_launch_plans(bits):
     rng = np.random.default_rng(300)
     prefix = [int(x) for x in rng.integers(30, 300, size=300)]
     w = W.make_workload("many", 8, prefix, "uniform", [16] * 300, 131072, seed=300)
-    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, 1, abi.PATH_AUTO) == 2
-    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, 4, abi.PATH_TC) == 3
+    kv_len = sum(w.prefix_lens) + w.total_q
+    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, kv_len, 1, abi.PATH_AUTO) == 2
+    assert abi.mla_tree_verify_launch_count(w.batch, w.total_q, w.heads, kv_len, 4, abi.PATH_TC) == 3
     ref = _oracle("many", w)
     out, lse = ref.attention()
     for splits in (1, 4):

@@ -163,8 +163,8 @@ enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI 
 // kTrBlocks key blocks of CTA 0, one thread per role, in
 // g_tc_trace[role][block][event]; read with mla_tree_tc_trace_read.
 enum { TR_PRODUCER, TR_MMA, TR_SENDER, TR_SOFTMAX, TR_RECEIVER, kTrRoles };
-constexpr int kTrBlocks = 1024, kTrEvents = 8;
 #ifdef MT_TC_TRACE
+constexpr int kTrBlocks = 1024, kTrEvents = 8;
 __device__ unsigned long long g_tc_trace[kTrRoles][kTrBlocks][kTrEvents];
 #define TC_TRACE(on, role, blk, ev)                                         \
   do {                                                                      \

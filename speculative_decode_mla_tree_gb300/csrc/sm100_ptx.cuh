@@ -103,11 +103,15 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitim
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = kWaitLimitNs) {
+  // the loops stay rolled: every wait site inlines this, and unrolled
+  // copies of the polling loop would crowd the instruction cache
+#pragma unroll 1
   for (int i = 0; i < 16; ++i)
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   if (*abort) return false;
   const uint64_t t0 = global_timer_ns();
   while (true) {
+#pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;

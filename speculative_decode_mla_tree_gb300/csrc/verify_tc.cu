@@ -88,11 +88,15 @@ constexpr int kKVLat = BN * 128;                      // one latent chunk of a s
 constexpr int kKVStage = 4 * kKVLat + BN * 64;        // 27648
 constexpr int kStages = 5;
 constexpr int kSX = kKV + kStages * kKVStage;         // the peer's fp32 partial scores of our rows, 2 buffers
-constexpr int kSXRow = BN * 4 + 16;                   // padded: rows land on different banks
-constexpr int kSXBytes = kOwnRows * kSXRow;
+// The exchange buffers are chunk-major: 16-byte chunk k of row r sits at
+// k * kXChunk + 16 r, so the 32 remote stores of one warp instruction (32
+// rows, one chunk each) fill 512 contiguous bytes, whole 32-byte sectors.
+constexpr int kXChunk = kOwnRows * 16;
+constexpr int kSXChunks = BN * 4 / 16;                // 12 chunks of 4 fp32 partial scores
+constexpr int kSXBytes = kSXChunks * kXChunk;
 constexpr int kPX = kSX + 2 * kSXBytes;               // the peer's P rows (+ running max, sums), 2 buffers
-constexpr int kPXRow = BN * 2 + 16;                   // P: 96 B; m at 96, l_0 at 100, l_1 at 104
-constexpr int kPXBytes = kOwnRows * kPXRow;
+constexpr int kPXChunks = BN * 2 / 16 + 1;            // 6 chunks of 8 bf16 P values, then m, l_0, l_1
+constexpr int kPXBytes = kPXChunks * kXChunk;
 constexpr int kMX = kPX + 2 * kPXBytes;               // half-row maxima [2][64][2] and sums [64][2]
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
 constexpr int kVis = kMX + (2 * kOwnRows * 2 + kOwnRows * 2) * 4;  // 2 x kVisNodes x 64-bit masks
@@ -123,7 +127,7 @@ constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for aligning the 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(BN % 16 == 0 && BN <= 64, "block width");
 static_assert(kQRope % 1024 == 0 && kQTail % 1024 == 0 && kKV % 1024 == 0 && kKVStage % 1024 == 0 && kSX % 16 == 0 &&
-                  kPX % 16 == 0 && kSXRow % 16 == 0 && kPXRow % 16 == 0 && kBars % 8 == 0 &&
+                  kPX % 16 == 0 && kBars % 8 == 0 &&
                   kMisc % 8 == 0,
               "alignment");
 
@@ -160,16 +164,16 @@ enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI 
 
 // Optional pipeline trace for studying the kernel (off unless the library
 // is compiled with -DMT_TC_TRACE): %globaltimer at fixed points of the first
-// kTrBlocks key blocks of CTA 0, one thread per role, in
-// g_tc_trace[role][block][event]; read with mla_tree_tc_trace_read.
+// kTrBlocks key blocks of the first cluster's two CTAs, one thread per role,
+// in g_tc_trace[cta][role][block][event]; read with mla_tree_tc_trace_read.
 enum { TR_PRODUCER, TR_MMA, TR_SENDER, TR_SOFTMAX, TR_RECEIVER, kTrRoles };
 #ifdef MT_TC_TRACE
-constexpr int kTrBlocks = 1024, kTrEvents = 8;
-__device__ unsigned long long g_tc_trace[kTrRoles][kTrBlocks][kTrEvents];
-#define TC_TRACE(on, role, blk, ev)                                         \
-  do {                                                                      \
-    if ((on) && blockIdx.x == 0 && (unsigned)(blk) < (unsigned)kTrBlocks)   \
-      g_tc_trace[role][blk][ev] = global_timer_ns();                        \
+constexpr int kTrCtas = 2, kTrBlocks = 1024, kTrEvents = 8;
+__device__ unsigned long long g_tc_trace[kTrCtas][kTrRoles][kTrBlocks][kTrEvents];
+#define TC_TRACE(on, role, blk, ev)                                              \
+  do {                                                                           \
+    if ((on) && blockIdx.x < kTrCtas && (unsigned)(blk) < (unsigned)kTrBlocks)   \
+      g_tc_trace[blockIdx.x][role][blk][ev] = global_timer_ns();                 \
   } while (0)
 #else
 #define TC_TRACE(on, role, blk, ev) \
@@ -672,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 64 * (int)(1u - cta) + rp;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float scale2 = a.sm_scale * kLog2e;
-    const uint32_t sx_peer = mapa(smem_u32(sm + kSX + rp * kSXRow), peer);
+    const uint32_t sx_peer = mapa(smem_u32(sm + kSX + rp * 16), peer);
     const uint32_t sxfull_peer0 = mapa(smem_u32(&bars[B_SX_FULL0]), peer);
     const bool tr = warp == (int)(2 - 2 * cta) && lane == 0;  // traced thread
     (void)tr;
@@ -748,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bar = sxfull_peer0 + 8 * b;
 #pragma unroll
           for (int q = 0; q < BN / 4; ++q)
-            st_async_v4(dst + 16 * q, __float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
+            st_async_v4(dst + kXChunk * q, __float_as_uint(x[4 * q]), __float_as_uint(x[4 * q + 1]),
                         __float_as_uint(x[4 * q + 2]), __float_as_uint(x[4 * q + 3]), bar);
         }
         TC_TRACE(tr, TR_SENDER, g, 1);
@@ -781,14 +785,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
         if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_RECEIVER, g, 0);
-        const uint8_t* px = sm + kPX + b * kPXBytes + rp * kPXRow;
+        const uint8_t* px = sm + kPX + b * kPXBytes + rp * 16;
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int q = 0; q < BN / 8; ++q) {
-          const uint4 u = *reinterpret_cast<const uint4*>(px + 16 * q);
+          const uint4 u = *reinterpret_cast<const uint4*>(px + kXChunk * q);
           pk[4 * q] = u.x; pk[4 * q + 1] = u.y; pk[4 * q + 2] = u.z; pk[4 * q + 3] = u.w;
         }
-        const uint4 ml = *reinterpret_cast<const uint4*>(px + BN * 2);
+        const uint4 ml = *reinterpret_cast<const uint4*>(px + kXChunk * (kPXChunks - 1));
         __syncwarp();
         if (lane == 0 && !dead && !*abort) {
           if (arms) mbar_arrive_expect_tx(&bars[B_PX_FULL0 + b], kPXTx);  // block g+2
@@ -885,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO + 128 * h;
     const uint32_t sxfree_peer0 = mapa(smem_u32(&bars[B_SX_FREE0]), peer);
-    const uint32_t px_peer = mapa(smem_u32(sm + kPX + ro * kPXRow), peer);
+    const uint32_t px_peer = mapa(smem_u32(sm + kPX + ro * 16), peer);
     const uint32_t pxfull_peer0 = mapa(smem_u32(&bars[B_PX_FULL0]), peer);
     const bool arms = warp == (int)(2 * cta) && lane == 0;   // re-arms SX_FULL
     const int pair_bar = 1 + (q4 & 1);                       // the row's two threads (64 in all)
@@ -1062,11 +1066,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the peer's partials of the same columns (already in the log2 domain)
         if (!dead) dead = !mbar_wait<true>(&bars[B_SX_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 1);
-        const uint8_t* sx = sm + kSX + b * kSXBytes + ro * kSXRow + 4 * kHalfCols * h;
+        const uint8_t* sx = sm + kSX + b * kSXBytes + ro * 16 + kXChunk * (kHalfCols / 4) * h;
         float s[kHalfCols];
 #pragma unroll
         for (int q = 0; q < kHalfCols / 4; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(sx + 16 * q);
+          const float4 v = *reinterpret_cast<const float4*>(sx + kXChunk * q);
           const float pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -1117,18 +1121,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         lh = lh * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+        TC_TRACE(arms, TR_SOFTMAX, g, 6);
 
         // the row's half of P, the running max and this half's sum to the
         // peer, once its receivers have taken block g-2 from that buffer
         if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FREE0 + b], ph ^ 1, abort, limit);
+        TC_TRACE(arms, TR_SOFTMAX, g, 7);
         if (!dead && !*abort) {
           const uint32_t dst = px_peer + b * kPXBytes;
           const uint32_t bar = pxfull_peer0 + 8 * b;
 #pragma unroll
           for (int q = 0; q < kHalfCols / 8; ++q)
-            st_async_v4(dst + 48 * h + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
-          if (h == 0) st_async_v2(dst + BN * 2, __float_as_uint(m), __float_as_uint(lh), bar);
-          else st_async_b32(dst + BN * 2 + 8, __float_as_uint(lh), bar);
+            st_async_v4(dst + kXChunk * (3 * h + q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3],
+                        bar);
+          const uint32_t ml = dst + kXChunk * (kPXChunks - 1);  // m, l_0 | l_1
+          if (h == 0) st_async_v2(ml, __float_as_uint(m), __float_as_uint(lh), bar);
+          else st_async_b32(ml + 8, __float_as_uint(lh), bar);
         }
         TC_TRACE(arms, TR_SOFTMAX, g, 3);
 

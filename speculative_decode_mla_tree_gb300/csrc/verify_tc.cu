@@ -168,7 +168,7 @@ enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI 
 // in g_tc_trace[cta][role][block][event]; read with mla_tree_tc_trace_read.
 enum { TR_PRODUCER, TR_MMA, TR_SENDER, TR_SOFTMAX, TR_RECEIVER, kTrRoles };
 #ifdef MT_TC_TRACE
-constexpr int kTrCtas = 2, kTrBlocks = 1024, kTrEvents = 8;
+constexpr int kTrCtas = 2, kTrBlocks = 1024, kTrEvents = 10;
 __device__ unsigned long long g_tc_trace[kTrCtas][kTrRoles][kTrBlocks][kTrEvents];
 #define TC_TRACE(on, role, blk, ev)                                              \
   do {                                                                           \
@@ -738,8 +738,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t s0[32], s1[16];
         const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b;
-        tmem_ld32(tsrc, s0);
-        tmem_ld16(tsrc + 32, s1);
+        tmem_ld32_nw(tsrc, s0);
+        tmem_ld16_nw(tsrc + 32, s1);
+        tmem_ld_wait();
+        tmem_regs_ready(s0);
+        tmem_regs_ready(s1);
         tc_fence_before();
         mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
         float x[BN];
@@ -990,6 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
         const int jb = it.j0 + blk * BN;
+        TC_TRACE(arms, TR_SOFTMAX, g, 8);
         uint64_t vm;
         if (kBits) {
           const uint32_t w0 = mnext[0], w1 = mnext[1], w2 = mnext[2];
@@ -1034,31 +1038,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
         }
         const uint32_t vh = (uint32_t)(vm >> (kHalfCols * h)) & ((1u << kHalfCols) - 1u);
+        TC_TRACE(arms, TR_SOFTMAX, g, 9);
 
         // this CTA's partial scores of the row's 24 columns, from TMEM
         if (!dead) dead = !mbar_wait<false>(&bars[B_S_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 0);
         tc_fence_after();
-        // naturally aligned pieces: columns [0, 16) + [16, 24) for h = 0,
-        // [24, 32) + [32, 48) for h = 1
+        // three naturally aligned 8-column pieces from column 24 h, one wait
         uint32_t own[kHalfCols];
         {
-          const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b;
-          uint32_t a16[16], a8[8];
-          if (h == 0) {
-            tmem_ld16(tsrc, a16);
-            tmem_ld8(tsrc + 16, a8);
+          const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b + kHalfCols * h;
+          uint32_t x0[8], x1[8], x2[8];
+          tmem_ld8_nw(tsrc, x0);
+          tmem_ld8_nw(tsrc + 8, x1);
+          tmem_ld8_nw(tsrc + 16, x2);
+          tmem_ld_wait();
+          tmem_regs_ready(x0);
+          tmem_regs_ready(x1);
+          tmem_regs_ready(x2);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) own[c] = a16[c];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) own[16 + c] = a8[c];
-          } else {
-            tmem_ld8(tsrc + 24, a8);
-            tmem_ld16(tsrc + 32, a16);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) own[c] = a8[c];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) own[8 + c] = a16[c];
+          for (int c = 0; c < 8; ++c) {
+            own[c] = x0[c];
+            own[8 + c] = x1[c];
+            own[16 + c] = x2[c];
           }
         }
         tc_fence_before();

@@ -42,9 +42,10 @@
 // Roles per CTA (384 threads): in CTA c, warps 0-7 whose TMEM lane quarter
 // holds the own rows run the softmax and the own rows' epilogue; of the
 // other warps 0-7, warps 0-3 send partial scores and warps 4-7 receive P
-// and run those rows' epilogue; warps 8-10 are TMA producers (one warp
-// alone issues tile::gather4 too slowly to keep up); warp 11 issues the
-// MMAs and owns TMEM. Every mbarrier wait is time-bounded: a timeout sets
+// and run those rows' epilogue; of warps 8-11, one issues the MMAs and owns
+// TMEM (warp 11 in CTA 0, warp 8 in CTA 1: a scheduler without softmax
+// warps) and the other three are TMA producers (one warp alone issues
+// tile::gather4 too slowly to keep up). Every mbarrier wait is time-bounded: a timeout sets
 // MT_DEV_TIMEOUT, after which no thread issues another copy, MMA or remote
 // store, every loop runs to its end (so no named barrier is left waiting)
 // and the copies and MMAs in flight are drained before TMEM is released.
@@ -69,9 +70,8 @@ constexpr int kOwnRows = BM / 2; // rows whose softmax a CTA runs
 constexpr int kHalfCols = BN / 2;  // columns per softmax thread (two threads per row)
 constexpr int kGatherLanes = BN / 4;  // four-row groups per block (tile::gather4)
 constexpr int kProducers = 3;    // TMA producer warps (one warp issues about 37 ns per gather4)
-constexpr int kFirstProducer = 8;
-constexpr int kMmaWarp = kFirstProducer + kProducers;
-constexpr int kThreads = 32 * (kMmaWarp + 1);
+constexpr int kFirstProducer = 8;  // warps 8-11: three producers and the MMA issuer
+constexpr int kThreads = 32 * (kFirstProducer + kProducers + 1);
 constexpr int kMaxBatch = 256;   // requests per launch (the plan lives in shared memory)
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
@@ -166,6 +166,9 @@ enum { PL_Q0, PL_N, PL_KV0, PL_L, PL_SPLITS, PL_LEN, PL_TILES, PL_M0LO, PL_M0HI 
 // is compiled with -DMT_TC_TRACE): %globaltimer at fixed points of the first
 // kTrBlocks key blocks of the first cluster's two CTAs, one thread per role,
 // in g_tc_trace[cta][role][block][event]; read with mla_tree_tc_trace_read.
+// Events 3-9 of the receiver role at block 0 mark the kernel's phases
+// (TC_MARK): entry, grid dependency resolved, plan ready, softmax and
+// receiver epilogues done, exit.
 enum { TR_PRODUCER, TR_MMA, TR_SENDER, TR_SOFTMAX, TR_RECEIVER, kTrRoles };
 #ifdef MT_TC_TRACE
 constexpr int kTrCtas = 2, kTrBlocks = 1024, kTrEvents = 10;
@@ -175,7 +178,11 @@ __device__ unsigned long long g_tc_trace[kTrCtas][kTrRoles][kTrBlocks][kTrEvents
     if ((on) && blockIdx.x < kTrCtas && (unsigned)(blk) < (unsigned)kTrBlocks)   \
       g_tc_trace[blockIdx.x][role][blk][ev] = global_timer_ns();                 \
   } while (0)
+#define TC_MARK(on, ev) TC_TRACE(on, TR_RECEIVER, 0, ev)
 #else
+#define TC_MARK(on, ev) \
+  do {                  \
+  } while (0)
 #define TC_TRACE(on, role, blk, ev) \
   do {                              \
   } while (0)
@@ -370,6 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();
   const uint32_t peer = cta ^ 1u;
+  // The MMA issuer polls without pause, so it sits on a scheduler (warp % 4)
+  // that runs none of the softmax warps: CTA 0's softmax rows are lane
+  // quarters 0-1 (schedulers 0-1), CTA 1's quarters 2-3.
+  const int mma_warp = cta ? kFirstProducer : kFirstProducer + kProducers;
   const int cluster_id = blockIdx.x >> 1;
   const uint64_t limit = p.limit_ns;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars[B_PX_FULL0 + s], kPXTx);
     }
   }
-  if (warp == kMmaWarp) {
+  if (warp == mma_warp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -427,13 +438,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Launched as a programmatic dependent of the kernel before it (the
   // marshaling of the same step): the set-up above overlaps that kernel's
   // tail; nothing it writes is read before it has completed.
+  TC_MARK(tid == 0, 3);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  TC_MARK(tid == 0, 4);
   // the last CTA publishes the split counts: with fewer items than clusters it
   // has none of its own, so the extra stores delay no item
   if (warp == 0) build_plan(p, plan, ord, obase, total_items_s, lane, blockIdx.x == gridDim.x - 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  TC_MARK(tid == 0, 5);
   // The peer's barriers must exist before anyone touches them remotely: every
   // thread arrives here, and the warps that reach into the peer wait before
   // their first remote access; the others wait at the end.
@@ -445,14 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t q_rows = (int64_t)a.total_q * H;
   const int64_t R = q_rows;
 
-  if (warp >= kFirstProducer && warp < kFirstProducer + kProducers) {
+  if (warp >= kFirstProducer && warp != mma_warp) {
     // ------------------------------------------------------------ producers
     // kProducers warps share every block's gathers: warp pw issues the
     // four-row groups [pw * kGroupsPerWarp, (pw + 1) * kGroupsPerWarp), one
     // group per lane, and completes its own barrier of the stage (so it can
     // drain exactly the copies it issued). The first producer warp also
     // loads the query tile's rope half.
-    const int pw = warp - kFirstProducer;
+    const int pw = warp - kFirstProducer - (mma_warp == kFirstProducer ? 1 : 0);
     const int grp = pw * kGroupsPerWarp + lane;
     const bool gathers = lane < kGroupsPerWarp;
     uint32_t kb = 0, qi = 0;
@@ -562,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t k = kb >= kStages ? kb - kStages : 0; k < kb; ++k)
         mbar_drain(&bars[B_KV_FULL0 + (k % kStages) * kProducers + pw], (k / kStages) & 1, kDrainNs);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t kb = 0, sc = 0, pc = 0, qi = 0, ii = 0;
@@ -878,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
+      TC_MARK(arms, 7);
     }
   } else {
     // ------------------------------------------------------------ softmax, epilogue (own rows)
@@ -1230,9 +1245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
+      TC_MARK(arms, 6);
     }
   }
 
+  TC_MARK(tid == 0, 8);
   if (warp >= kFirstProducer) cluster_wait();  // pairs with the arrival after set-up
   // this CTA's outputs are issued: the merge kernel (launched as a dependent
   // grid) may start its set-up; it waits for this grid's completion before
@@ -1247,7 +1264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == mma_warp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

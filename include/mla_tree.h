@@ -354,7 +354,7 @@ int mla_tree_verify_validate(const mt_bf16* q, const mt_bf16* kv_buf, int64_t nu
  *     batch, total_q, heads, max_splits) exceeds MT_NOALLOC_SCRATCH_BYTES is
  *     rejected with MT_ESCRATCH before anything is launched.
  *   - The first call on a device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture.
+ *     array's device address with a runtime query.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing in it needs clearing). Calls that may overlap on the
  *     GPU -- unordered streams -- race on it; order them.

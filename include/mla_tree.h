@@ -234,9 +234,10 @@ int mla_tree_test_wait_limits(int drop_item, int64_t wait_limit_ns);
  * A row with no visible position gets out = 0 and lse = -inf.
  * Arithmetic: every score is an fp32 sum of bf16 products (the tensor-core
  * kernel adds its two CTAs' fp32 partial sums); the online softmax runs in
- * fp32 in the log2 domain; the weights are rounded to bf16 for the P.V
- * product and the denominator sums those same bf16 weights; split partials
- * are fp32. Nothing narrower than fp32 holds a score or a partial output.
+ * fp32 in the log2 domain; the tensor-core kernel rounds the weights to bf16
+ * for its P.V product and sums those same bf16 weights in the denominator,
+ * the warp-shuffle kernel keeps them in fp32; split partials are fp32.
+ * Nothing narrower than fp32 holds a score or a partial output.
  *   q:       bf16 [total_q, heads, 576], 16-byte aligned
  *   kv_buf:  bf16 [num_slots, 576], 16-byte aligned (rows of 1152 bytes)
  *   kv_indices: int32 [kv_indices_len]; kv_indptr, qo_indptr: int32 [batch+1]

@@ -24,7 +24,7 @@
 //             CTA owns (64 rows x 48) to that CTA
 //   softmax   the owner adds the two fp32 partials (exact scores of its
 //             rows, in the log2 domain), applies the tree mask and runs the
-//             online softmax (two threads per row, 24 columns each; lazy
+//             online softmax (four threads per row, 12 columns each; lazy
 //             rescaling: the running max moves only when it grows by more
 //             than 8, i.e. a factor of 256); it writes its rows of P (bf16)
 //             to its own TMEM and sends them, with the running max and
@@ -39,13 +39,14 @@
 // shared memory) and two score buffers. The scores cross between the CTAs
 // in fp32, so no partial is rounded below fp32 before the softmax.
 //
-// Roles per CTA (384 threads): in CTA c, warps 0-7 whose TMEM lane quarter
-// holds the own rows run the softmax and the own rows' epilogue; of the
-// other warps 0-7, warps 0-3 send partial scores and warps 4-7 receive P
-// and run those rows' epilogue; of warps 8-11, one issues the MMAs and owns
-// TMEM (warp 11 in CTA 0, warp 8 in CTA 1: a scheduler without softmax
-// warps) and the other three are TMA producers (one warp alone issues
-// tile::gather4 too slowly to keep up). Every mbarrier wait is time-bounded: a timeout sets
+// Roles per CTA (512 threads, 16 warps; a warp's TMEM lane quarter and its
+// scheduler are warp % 4): in CTA c the eight warps whose quarter holds the
+// own rows run the softmax (four threads per row) and the own rows'
+// epilogue, so the own rows' two schedulers run nothing else. On the other
+// two schedulers, warps 0-3 send partial scores, warps 4-7 receive P and run
+// those rows' epilogue, and of warps 8-15 one issues the MMAs and owns TMEM
+// while three are TMA producers (one warp alone issues tile::gather4 too
+// slowly to keep up). Every mbarrier wait is time-bounded: a timeout sets
 // MT_DEV_TIMEOUT, after which no thread issues another copy, MMA or remote
 // store, every loop runs to its end (so no named barrier is left waiting)
 // and the copies and MMAs in flight are drained before TMEM is released.
@@ -67,11 +68,13 @@ using namespace sm100;
 constexpr int BM = 128;          // tile rows = TMEM lanes
 constexpr int BN = 48;           // key rows per block
 constexpr int kOwnRows = BM / 2; // rows whose softmax a CTA runs
-constexpr int kHalfCols = BN / 2;  // columns per softmax thread (two threads per row)
+constexpr int kRowThreads = 4;   // softmax threads per own row, in four warps of the row's quarter
+constexpr int kQCols = BN / kRowThreads;  // columns per softmax thread
+constexpr int kSoftThreads = kOwnRows * kRowThreads;  // 256
 constexpr int kGatherLanes = BN / 4;  // four-row groups per block (tile::gather4)
 constexpr int kProducers = 3;    // TMA producer warps (one warp issues about 37 ns per gather4)
-constexpr int kFirstProducer = 8;  // warps 8-11: three producers and the MMA issuer
-constexpr int kThreads = 32 * (kFirstProducer + kProducers + 1);
+constexpr int kThreads = 512;    // 16 warps
+static_assert(kProducers == 3, "warps 8-15 of the two non-softmax quarters: one MMA issuer, three producers");
 constexpr int kMaxBatch = 256;   // requests per launch (the plan lives in shared memory)
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
@@ -95,11 +98,15 @@ constexpr int kXChunk = kOwnRows * 16;
 constexpr int kSXChunks = BN * 4 / 16;                // 12 chunks of 4 fp32 partial scores
 constexpr int kSXBytes = kSXChunks * kXChunk;
 constexpr int kPX = kSX + 2 * kSXBytes;               // the peer's P rows (+ running max, sums), 2 buffers
-constexpr int kPXChunks = BN * 2 / 16 + 1;            // 6 chunks of 8 bf16 P values, then m, l_0, l_1
-constexpr int kPXBytes = kPXChunks * kXChunk;
-constexpr int kMX = kPX + 2 * kPXBytes;               // half-row maxima [2][64][2] and sums [64][2]
+// P rows go in 8-byte chunks (a softmax thread's 12 keys are 24 bytes): chunk
+// k of row r at k * kPChunk + 8 r; chunks 0..11 hold P, chunk 12 + h holds
+// (m, l_h) of the row's thread h
+constexpr int kPChunk = kOwnRows * 8;
+constexpr int kPXChunks = BN * 2 / 8 + kRowThreads;   // 16
+constexpr int kPXBytes = kPXChunks * kPChunk;
+constexpr int kMX = kPX + 2 * kPXBytes;               // quarter-row maxima [2][64][4] and sums [64][4]
 constexpr int kVisNodes = BM + 2;                     // distinct draft nodes a tile can touch
-constexpr int kVis = kMX + (2 * kOwnRows * 2 + kOwnRows * 2) * 4;  // 2 x kVisNodes x 64-bit masks
+constexpr int kVis = kMX + (2 * kOwnRows * kRowThreads + kOwnRows * kRowThreads) * 4;  // 2 x kVisNodes x 64-bit masks
 constexpr int kBars = kVis + 2 * kVisNodes * 8;
 constexpr int B_Q_FULL = 0;                     // query rope half landed (TMA)
 constexpr int B_QT_FULL = 1;                    // query latent half written to TMEM
@@ -134,7 +141,7 @@ static_assert(kQRope % 1024 == 0 && kQTail % 1024 == 0 && kKV % 1024 == 0 && kKV
 constexpr uint32_t kQTx = 2 * BM * 64;                // query rope + latent-tail bytes per CTA per item
 constexpr uint32_t kKVTxWarp = kGroupsPerWarp * 4 * (4 * 128 + 64);  // key bytes per producer warp per block
 constexpr uint32_t kSXTx = kOwnRows * BN * 4;         // partial-score bytes into a CTA per block
-constexpr uint32_t kPXTx = kOwnRows * (BN * 2 + 12);  // P + m + l_0 + l_1 bytes into a CTA per block
+constexpr uint32_t kPXTx = kPXBytes;                  // P + (m, l_h) bytes into a CTA per block
 static_assert(kKVTxWarp * kProducers == (uint32_t)kKVStage, "stage bytes");
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns (512 x 128 lanes; lane = tile row):
@@ -361,6 +368,22 @@ __device__ void build_plan(const TcParams& p, int* plan, int* ord, int* obase, i
   }
 }
 
+// A softmax thread's 28 query columns into TMEM as three naturally aligned
+// pieces: 16 columns at O16, 8 at O8, 4 at O4 (offsets within the 28).
+template <int O16, int O8, int O4>
+__device__ __forceinline__ void tmem_st_q28(uint32_t tq, const uint32_t (&w)[28]) {
+  uint32_t a16[16], a8[8], a4[4];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a16[k] = w[O16 + k];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a8[k] = w[O8 + k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a4[k] = w[O4 + k];
+  tmem_st16(tq + O16, a16);
+  tmem_st8(tq + O8, a8);
+  tmem_st4(tq + O4, a4);
+}
+
 // kBits: the tree mask is in the bit form (rows of ceil(L / 32) words)
 // kSkip: prefix columns are visible and their mask entries are not read
 template <bool kBits, bool kSkip>
@@ -377,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();
   const uint32_t peer = cta ^ 1u;
-  // The MMA issuer polls without pause, so it sits on a scheduler (warp % 4)
-  // that runs none of the softmax warps: CTA 0's softmax rows are lane
-  // quarters 0-1 (schedulers 0-1), CTA 1's quarters 2-3.
-  const int mma_warp = cta ? kFirstProducer : kFirstProducer + kProducers;
+  // Warps 8-15 on the two schedulers that run no softmax warp (CTA 0's own
+  // rows are lane quarters 0-1, CTA 1's quarters 2-3): the first issues the
+  // MMAs, the other three produce.
+  const int mma_warp = cta ? 8 : 10;
   const int cluster_id = blockIdx.x >> 1;
   const uint64_t limit = p.limit_ns;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -391,12 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* ord = reinterpret_cast<int*>(sm + kOrd);
   int* obase = reinterpret_cast<int*>(sm + kOBase);
   uint64_t* vis = reinterpret_cast<uint64_t*>(sm + kVis);
-  float* mxs = reinterpret_cast<float*>(sm + kMX);               // [2][64][2] half-row maxima
-  float* lxs = mxs + 2 * kOwnRows * 2;                           // [64][2] half-row sums
+  float* mxs = reinterpret_cast<float*>(sm + kMX);               // [2][64][4] quarter-row maxima
+  float* lxs = mxs + 2 * kOwnRows * kRowThreads;                 // [64][4] quarter-row sums
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    mbar_init(&bars[B_QT_FULL], 128 + 64);            // softmax threads + senders
+    mbar_init(&bars[B_QT_FULL], kSoftThreads + 64);   // softmax threads + senders
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int s = 0; s < kStages; ++s) {
       for (int w = 0; w < kProducers; ++w) mbar_init(&bars[B_KV_FULL0 + s * kProducers + w], 1);
@@ -404,17 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[B_S_FULL0 + s], 1);
-      mbar_init(&bars[B_S_EMPTY0 + s], 128 + 64);     // softmax threads + senders
+      mbar_init(&bars[B_S_EMPTY0 + s], kSoftThreads + 64);  // softmax threads + senders
       mbar_init(&bars[B_SX_FULL0 + s], 1);            // armed once per block, + the peer's bytes
-      mbar_init(&bars[B_SX_FREE0 + s], 4);            // the peer's four softmax warps
+      mbar_init(&bars[B_SX_FREE0 + s], kSoftThreads / 32);  // the peer's softmax warps
       mbar_init(&bars[B_PX_FULL0 + s], 1);
       mbar_init(&bars[B_PX_FREE0 + s], 2);            // the peer's two receiver warps
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[B_P_FULL0 + s], 128 + 64);      // softmax threads + receivers
+      mbar_init(&bars[B_P_FULL0 + s], kSoftThreads + 64);  // softmax threads + receivers
       mbar_init(&bars[B_O_DONE0 + s], 1);
     }
-    mbar_init(&bars[B_O_FREE], 128 + 64);
+    mbar_init(&bars[B_O_FREE], kSoftThreads + 64);
     mbar_init(&bars[B_DRAIN], 1);
     *abort = 0;
     fence_mbar_init_cluster();
@@ -430,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kFirstProducer && lane == 0) {
+  if (warp == 9 && lane == 0) {
     prefetch_tmap(&tm_qrope);
     prefetch_tmap(&tm_kvlat);
     prefetch_tmap(&tm_kvrope);
@@ -456,17 +479,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_items = *total_items_s;
   const int q4 = warp & 3;                       // TMEM lane quarter of this warp
   const bool own_quarter = (uint32_t)(q4 >> 1) == cta;
+  const int wg = warp >> 2;
+  const bool is_mma = warp == mma_warp;
+  const bool is_producer = !own_quarter && wg >= 2 && !is_mma;
   const int64_t q_rows = (int64_t)a.total_q * H;
   const int64_t R = q_rows;
 
-  if (warp >= kFirstProducer && warp != mma_warp) {
+  if (is_producer) {
     // ------------------------------------------------------------ producers
     // kProducers warps share every block's gathers: warp pw issues the
     // four-row groups [pw * kGroupsPerWarp, (pw + 1) * kGroupsPerWarp), one
     // group per lane, and completes its own barrier of the stage (so it can
     // drain exactly the copies it issued). The first producer warp also
     // loads the query tile's rope half.
-    const int pw = warp - kFirstProducer - (mma_warp == kFirstProducer ? 1 : 0);
+    const int pw = (wg - 2) * 2 + (q4 & 1) - 1;  // the MMA issuer is the first of the four
     const int grp = pw * kGroupsPerWarp + lane;
     const bool gathers = lane < kGroupsPerWarp;
     uint32_t kb = 0, qi = 0;
@@ -576,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t k = kb >= kStages ? kb - kStages : 0; k < kb; ++k)
         mbar_drain(&bars[B_KV_FULL0 + (k % kStages) * kProducers + pw], (k / kStages) & 1, kDrainNs);
     }
-  } else if (warp == mma_warp) {
+  } else if (is_mma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t kb = 0, sc = 0, pc = 0, qi = 0, ii = 0;
@@ -679,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[B_DRAIN]);  // everything issued has completed before TMEM is freed
       mbar_drain(&bars[B_DRAIN], 0, kDrainNs);
     }
-  } else if (!own_quarter && warp < 4) {
+  } else if (!own_quarter && wg == 0) {
     // ------------------------------------------------------------ score senders
     // Thread rp owns tile row 64 (1 - c) + rp, which the peer's softmax
     // runs. Per item it writes that row's latent query half into TMEM (QK's
@@ -775,10 +801,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         TC_TRACE(tr, TR_SENDER, g, 1);
       }
     }
-  } else if (!own_quarter) {
+  } else if (!own_quarter) {  // wg == 1
     // ------------------------------------------------------------ P receivers
     // Thread rp owns tile row 64 (1 - c) + rp. Per block it takes that row's
-    // P (bf16), running max and half sums from the peer's message, rescales
+    // P (bf16), running max and quarter sums from the peer's message, rescales
     // this CTA's half of the row of O when the max moved, and writes P into
     // TMEM for the P.V MMA. After an item it writes the row's output half.
     const int rp = (q4 - 2 * (int)(1u - cta)) * 32 + lane;
@@ -797,27 +823,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0, id = item_of(0, cluster_id, p.nclusters); id < total_items;
          id = item_of(++rnd, cluster_id, p.nclusters)) {
       const Item it = decode_item(plan, ord, obase, a.batch, id);
-      float m_prev = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float m_prev = -INFINITY, lsum = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
         if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_RECEIVER, g, 0);
-        const uint8_t* px = sm + kPX + b * kPXBytes + rp * 16;
+        const uint8_t* px = sm + kPX + b * kPXBytes + rp * 8;
         uint32_t pk[BN / 2];
 #pragma unroll
-        for (int q = 0; q < BN / 8; ++q) {
-          const uint4 u = *reinterpret_cast<const uint4*>(px + kXChunk * q);
-          pk[4 * q] = u.x; pk[4 * q + 1] = u.y; pk[4 * q + 2] = u.z; pk[4 * q + 3] = u.w;
+        for (int q = 0; q < BN / 4; ++q) {
+          const uint2 u = *reinterpret_cast<const uint2*>(px + kPChunk * q);
+          pk[2 * q] = u.x;
+          pk[2 * q + 1] = u.y;
         }
-        const uint4 ml = *reinterpret_cast<const uint4*>(px + kXChunk * (kPXChunks - 1));
+        uint2 ml[kRowThreads];  // (m, l_h) from each of the owner's four threads
+#pragma unroll
+        for (int q = 0; q < kRowThreads; ++q) ml[q] = *reinterpret_cast<const uint2*>(px + kPChunk * (BN / 4 + q));
         __syncwarp();
         if (lane == 0 && !dead && !*abort) {
           if (arms) mbar_arrive_expect_tx(&bars[B_PX_FULL0 + b], kPXTx);  // block g+2
           mbar_arrive_remote_relaxed(pxfree_peer0 + 8 * b);
         }
-        const float m_new = __uint_as_float(ml.x);
-        l0 = __uint_as_float(ml.y);
-        l1 = __uint_as_float(ml.z);
+        const float m_new = __uint_as_float(ml[0].x);
+        lsum = (__uint_as_float(ml[0].y) + __uint_as_float(ml[1].y)) +
+               (__uint_as_float(ml[2].y) + __uint_as_float(ml[3].y));
         // the owner rescales its half of O by exactly this factor: same
         // inputs to the same instruction
         const bool resc = blk > 0 && __float_as_uint(m_new) != __float_as_uint(m_prev);
@@ -858,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // owner's final sum, once the item's last P.V is done
       wait_pv(g - 1);
       tc_fence_after();
-      const float l = l0 + l1;
+      const float l = lsum;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int rows_req = it.n * H;
       const bool valid = it.row0 + r < rows_req;
@@ -896,21 +925,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax, epilogue (own rows)
-    // Two threads per own row: h = 0 takes columns [0, 24) of every block,
-    // h = 1 columns [24, 48). Block g's peer partials arrive in SX buffer
-    // g & 1; the row's P goes to this CTA's TMEM and to the peer's PX
-    // buffer g & 1.
-    const int h = warp >> 2;
+    // Four threads per own row, in the four warps of the row's lane quarter:
+    // thread h takes columns [12 h, 12 h + 12) of every block and dims
+    // [64 h, 64 h + 64) of this CTA's half of O. Block g's peer partials
+    // arrive in SX buffer g & 1; the row's P goes to this CTA's TMEM and to
+    // the peer's PX buffer g & 1.
+    const int h = wg;
     const int ro = (q4 - 2 * (int)cta) * 32 + lane;
     const int r = 64 * (int)cta + ro;
-    const int st_idx = 64 * h + ro;                  // 0..127 over the softmax threads
+    const int st_idx = 64 * h + ro;                  // 0..255 over the softmax threads
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const uint32_t t_o = tmem + lane_base + kTmemO + 128 * h;
+    const uint32_t t_o = tmem + lane_base + kTmemO + 64 * h;
     const uint32_t sxfree_peer0 = mapa(smem_u32(&bars[B_SX_FREE0]), peer);
-    const uint32_t px_peer = mapa(smem_u32(sm + kPX + ro * 16), peer);
+    const uint32_t px_peer = mapa(smem_u32(sm + kPX + ro * 8), peer);
     const uint32_t pxfull_peer0 = mapa(smem_u32(&bars[B_PX_FULL0]), peer);
     const bool arms = warp == (int)(2 * cta) && lane == 0;   // re-arms SX_FULL
-    const int pair_bar = 1 + (q4 & 1);                       // the row's two threads (64 in all)
+    const int quad_bar = 1 + (q4 & 1);                       // the rows' four warps (128 threads)
     const float scale2 = a.sm_scale * kLog2e;
     uint32_t g = 0, qi = 0;
     bool dead = false;
@@ -921,34 +951,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // this row's share of the query's latent dims 0..223 into TMEM for item
-    // `id`: h = 0 writes dims 0..127, h = 1 dims 128..223
+    // `id`: thread h writes dims [56 h, 56 h + 56), TMEM columns
+    // [28 h, 28 h + 28) of the query block
     auto load_q = [&](int id) {
       const Item it = decode_item(plan, ord, obase, a.batch, id);
       const int64_t qrow = (int64_t)it.q0 * H + it.row0 + r;
-      const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * kDqk + 256 * cta + 128 * h);
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * kDqk + 256 * cta + 56 * h);
       const bool in = qrow < q_rows;
-      const int nv = h == 0 ? 16 : 12;
-      uint4 v[16];
+      uint4 v[7];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = in && k < nv ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < 7; ++k) v[k] = in ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
       if (!dead) dead = !mbar_wait<false>(&bars[B_Q_EMPTY], (qi & 1) ^ 1, abort, limit);
       ++qi;
       tc_fence_after();
-      uint32_t w0[32], w1[32];
+      uint32_t w[28];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        w0[4 * k] = v[k].x; w0[4 * k + 1] = v[k].y; w0[4 * k + 2] = v[k].z; w0[4 * k + 3] = v[k].w;
-        w1[4 * k] = v[8 + k].x; w1[4 * k + 1] = v[8 + k].y;
-        w1[4 * k + 2] = v[8 + k].z; w1[4 * k + 3] = v[8 + k].w;
+      for (int k = 0; k < 7; ++k) {
+        w[4 * k] = v[k].x; w[4 * k + 1] = v[k].y; w[4 * k + 2] = v[k].z; w[4 * k + 3] = v[k].w;
       }
-      tmem_st32(tmem + lane_base + kTmemQ + 64 * h, w0);
-      if (h == 0) {
-        tmem_st32(tmem + lane_base + kTmemQ + 32, w1);
-      } else {
-        uint32_t w16[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) w16[k] = w1[k];
-        tmem_st16(tmem + lane_base + kTmemQ + 96, w16);
+      const uint32_t tq = tmem + lane_base + kTmemQ + 28 * h;
+      switch (h) {  // pieces of 16, 8 and 4 columns, each at a multiple of its width
+        case 0: tmem_st_q28<0, 16, 24>(tq, w); break;
+        case 1: tmem_st_q28<4, 20, 0>(tq, w); break;
+        case 2: tmem_st_q28<8, 0, 24>(tq, w); break;
+        default: tmem_st_q28<12, 4, 0>(tq, w); break;
       }
       tmem_st_wait();
       tc_fence_before();
@@ -966,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pre = kSkip ? it.L - it.n : 0;  // prefix columns: visible, mask unread
       // Byte mask: the bits of a block arrive as (draft node, 8-column
       // group) pairs over the nodes of the own rows; softmax thread st_idx
-      // owns pairs st_idx + 128 k. When the own rows touch few enough nodes
+      // owns pairs st_idx + 256 k. When the own rows touch few enough nodes
       // (every case with 4 or more heads), the bytes of block blk+1 are
       // loaded while block blk is processed.
       const int own0 = min(it.row0 + 64 * (int)cta, rows_req - 1);
@@ -975,13 +1001,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cnt = max(1, i_hi - i_lo + 1);
       constexpr int kGroups = BN / 8;  // 8-column groups per block row
       const int pairs = cnt * kGroups;
-      const bool prefetch = pairs <= 128 * kMaskPrefetch;
+      const bool prefetch = pairs <= kSoftThreads * kMaskPrefetch;
       uint8_t raw[kMaskPrefetch][8];
       auto load_mask = [&](int blk_) {
         const int jb_ = it.j0 + blk_ * BN;
 #pragma unroll
         for (int k = 0; k < kMaskPrefetch; ++k) {
-          const int q = st_idx + 128 * k;
+          const int q = st_idx + kSoftThreads * k;
           if (q < pairs) {
             const int pos0 = jb_ + 8 * (q % kGroups);
             const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
@@ -1024,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (prefetch) {
 #pragma unroll
             for (int k = 0; k < kMaskPrefetch; ++k) {
-              const int q = st_idx + 128 * k;
+              const int q = st_idx + kSoftThreads * k;
               if (q < pairs) {
                 uint32_t bits = 0;
 #pragma unroll
@@ -1034,7 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (blk + 1 < it.nblocks) load_mask(blk + 1);
           } else {
-            for (int q = st_idx; q < pairs; q += 128) {
+            for (int q = st_idx; q < pairs; q += kSoftThreads) {
               const int pos0 = jb + 8 * (q % kGroups);
               const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
               uint32_t bits = 0;
@@ -1044,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
             }
           }
-          named_bar_sync(3, 128);
+          named_bar_sync(3, kSoftThreads);
           const int ni = node - i_lo;
           vm = (ni >= 0 && ni < cnt) ? vis[b * kVisNodes + ni] : 0ull;
         }
@@ -1052,30 +1078,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pc = min(pre, it.j1) - jb;
           vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
         }
-        const uint32_t vh = (uint32_t)(vm >> (kHalfCols * h)) & ((1u << kHalfCols) - 1u);
+        const uint32_t vh = (uint32_t)(vm >> (kQCols * h)) & ((1u << kQCols) - 1u);
         TC_TRACE(arms, TR_SOFTMAX, g, 9);
 
-        // this CTA's partial scores of the row's 24 columns, from TMEM
+        // this CTA's partial scores of the row's 12 columns, from TMEM
         if (!dead) dead = !mbar_wait<false>(&bars[B_S_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 0);
         tc_fence_after();
-        // three naturally aligned 8-column pieces from column 24 h, one wait
-        uint32_t own[kHalfCols];
+        // naturally aligned pieces from column 12 h, one wait: 8 + 4 columns
+        // for even h, 4 + 8 for odd h
+        uint32_t own[kQCols];
         {
-          const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b + kHalfCols * h;
-          uint32_t x0[8], x1[8], x2[8];
-          tmem_ld8_nw(tsrc, x0);
-          tmem_ld8_nw(tsrc + 8, x1);
-          tmem_ld8_nw(tsrc + 16, x2);
+          const uint32_t tsrc = tmem + lane_base + kTmemS + 64 * b + kQCols * h;
+          uint32_t x8[8], x4[4];
+          if ((h & 1) == 0) {
+            tmem_ld8_nw(tsrc, x8);
+            tmem_ld4_nw(tsrc + 8, x4);
+          } else {
+            tmem_ld4_nw(tsrc, x4);
+            tmem_ld8_nw(tsrc + 4, x8);
+          }
           tmem_ld_wait();
-          tmem_regs_ready(x0);
-          tmem_regs_ready(x1);
-          tmem_regs_ready(x2);
+          tmem_regs_ready(x8);
+          tmem_regs_ready(x4);
+          if ((h & 1) == 0) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            own[c] = x0[c];
-            own[8 + c] = x1[c];
-            own[16 + c] = x2[c];
+            for (int c = 0; c < 8; ++c) own[c] = x8[c];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) own[8 + c] = x4[c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) own[c] = x4[c];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) own[4 + c] = x8[c];
           }
         }
         tc_fence_before();
@@ -1083,10 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the peer's partials of the same columns (already in the log2 domain)
         if (!dead) dead = !mbar_wait<true>(&bars[B_SX_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 1);
-        const uint8_t* sx = sm + kSX + b * kSXBytes + ro * 16 + kXChunk * (kHalfCols / 4) * h;
-        float s[kHalfCols];
+        const uint8_t* sx = sm + kSX + b * kSXBytes + ro * 16 + kXChunk * (kQCols / 4) * h;
+        float s[kQCols];
 #pragma unroll
-        for (int q = 0; q < kHalfCols / 4; ++q) {
+        for (int q = 0; q < kQCols / 4; ++q) {
           const float4 v = *reinterpret_cast<const float4*>(sx + kXChunk * q);
           const float pv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -1101,19 +1136,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_remote_relaxed(sxfree_peer0 + 8 * b);
         }
 
-        // masked maximum of the half row, then of the row
+        // masked maximum of the quarter row, then of the row
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kHalfCols; ++c) {
+        for (int c = 0; c < kQCols; ++c) {
           const float v = (vh >> c) & 1u ? s[c] : -INFINITY;
           s[c] = v;
           mx4[c & 3] = fmaxf(mx4[c & 3], v);
         }
         const float mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        mxs[(b * kOwnRows + ro) * 2 + h] = mxh;
-        named_bar_sync(pair_bar, 64);
+        float* mrow = mxs + (b * kOwnRows + ro) * kRowThreads;
+        mrow[h] = mxh;
+        named_bar_sync(quad_bar, 128);
         TC_TRACE(arms, TR_SOFTMAX, g, 2);
-        const float mb = fmaxf(mxh, mxs[(b * kOwnRows + ro) * 2 + (h ^ 1)]);
+        const float4 m4 = *reinterpret_cast<const float4*>(mrow);
+        const float mb = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
         float corr = 1.f;
         bool resc = false;
         if (mb > m + kRescale) {
@@ -1122,13 +1159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[kHalfCols / 2];
+        uint32_t pk[kQCols / 2];
         if (m == -INFINITY) {
 #pragma unroll
-          for (int c = 0; c < kHalfCols / 2; ++c) pk[c] = 0u;
+          for (int c = 0; c < kQCols / 2; ++c) pk[c] = 0u;
         } else {
 #pragma unroll
-          for (int c = 0; c < kHalfCols / 2; ++c) {
+          for (int c = 0; c < kQCols / 2; ++c) {
             const float p0 = ex2_approx(s[2 * c] - m), p1 = ex2_approx(s[2 * c + 1] - m);
             const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
             // the denominator sums the same bf16 weights the P.V product uses,
@@ -1140,20 +1177,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         lh = lh * corr + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
         TC_TRACE(arms, TR_SOFTMAX, g, 6);
 
-        // the row's half of P, the running max and this half's sum to the
-        // peer, once its receivers have taken block g-2 from that buffer
+        // the row's quarter of P, the running max and this quarter's sum to
+        // the peer, once its receivers have taken block g-2 from that buffer
         if (!dead) dead = !mbar_wait<true>(&bars[B_PX_FREE0 + b], ph ^ 1, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 7);
         if (!dead && !*abort) {
           const uint32_t dst = px_peer + b * kPXBytes;
           const uint32_t bar = pxfull_peer0 + 8 * b;
 #pragma unroll
-          for (int q = 0; q < kHalfCols / 8; ++q)
-            st_async_v4(dst + kXChunk * (3 * h + q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3],
-                        bar);
-          const uint32_t ml = dst + kXChunk * (kPXChunks - 1);  // m, l_0 | l_1
-          if (h == 0) st_async_v2(ml, __float_as_uint(m), __float_as_uint(lh), bar);
-          else st_async_b32(ml + 8, __float_as_uint(lh), bar);
+          for (int q = 0; q < kQCols / 4; ++q)
+            st_async_v2(dst + kPChunk * (3 * h + q), pk[2 * q], pk[2 * q + 1], bar);
+          st_async_v2(dst + kPChunk * (BN / 4 + h), __float_as_uint(m), __float_as_uint(lh), bar);
         }
         TC_TRACE(arms, TR_SOFTMAX, g, 3);
 
@@ -1168,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (any_need) {
           const float f = need ? corr : 1.f;
 #pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
             uint32_t o[32];
             tmem_ld32(t_o + 32 * k, o);
 #pragma unroll
@@ -1176,22 +1210,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(t_o + 32 * k, o);
           }
         }
-        if (h == 0) {  // keys 0-15 -> piece 0, keys 16-23 -> first half of piece 1
-          uint32_t x8[8], x4[4];
+        // the quarter's 6 bf16 pairs (keys 12h .. 12h+11) at P word 6h of the
+        // buffer: pieces of 4 and 2 columns, each at a multiple of its width
+        {
+          const uint32_t pb = g & 1;
+          uint32_t x4[4], x2[2];
+          if ((h & 1) == 0) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) x8[c] = pk[c];
+            for (int c = 0; c < 4; ++c) x4[c] = pk[c];
+            x2[0] = pk[4];
+            x2[1] = pk[5];
+            const uint32_t c4 = h == 0 ? tmem_p_col(pb, 0) : tmem_p_col(pb, 1) + 4;
+            const uint32_t c2 = h == 0 ? tmem_p_col(pb, 0) + 4 : tmem_p_col(pb, 2);
+            tmem_st4(tmem + lane_base + c4, x4);
+            tmem_st2(tmem + lane_base + c2, x2);
+          } else {
+            x2[0] = pk[0];
+            x2[1] = pk[1];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) x4[c] = pk[8 + c];
-          tmem_st8(tmem + lane_base + tmem_p_col(g & 1, 0), x8);
-          tmem_st4(tmem + lane_base + tmem_p_col(g & 1, 1), x4);
-        } else {       // keys 24-31 -> second half of piece 1, keys 32-47 -> piece 2
-          uint32_t x4[4], x8[8];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) x4[c] = pk[c];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) x8[c] = pk[4 + c];
-          tmem_st4(tmem + lane_base + tmem_p_col(g & 1, 1) + 4, x4);
-          tmem_st8(tmem + lane_base + tmem_p_col(g & 1, 2), x8);
+            for (int c = 0; c < 4; ++c) x4[c] = pk[2 + c];
+            const uint32_t c2 = h == 1 ? tmem_p_col(pb, 0) + 6 : tmem_p_col(pb, 2) + 2;
+            const uint32_t c4 = h == 1 ? tmem_p_col(pb, 1) : tmem_p_col(pb, 2) + 4;
+            tmem_st2(tmem + lane_base + c2, x2);
+            tmem_st4(tmem + lane_base + c4, x4);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1203,20 +1245,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int next = item_of(rnd + 1, cluster_id, p.nclusters);
       if (next < total_items) load_q(next);
 
-      // epilogue: O / l for the row's 128 dims of this CTA's half, and the LSE
-      lxs[ro * 2 + h] = lh;
-      named_bar_sync(pair_bar, 64);
-      const float l = lxs[ro * 2] + lxs[ro * 2 + 1];
+      // epilogue: O / l for the row's 64 dims of this CTA's half, and the LSE
+      lxs[ro * kRowThreads + h] = lh;
+      named_bar_sync(quad_bar, 128);
+      const float4 l4 = *reinterpret_cast<const float4*>(lxs + ro * kRowThreads);
+      const float l = (l4.x + l4.y) + (l4.z + l4.w);
       wait_pv(g - 1);  // the item's last P.V
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t grow = (int64_t)it.q0 * H + row;
 #pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 2; ++k) {
         uint32_t o[32];
         tmem_ld32(t_o + 32 * k, o);
         if (!valid) continue;
-        const int col = 256 * (int)cta + 128 * h + 32 * k;
+        const int col = 256 * (int)cta + 64 * h + 32 * k;
         if (it.splits == 1) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + grow * kDv + col);
 #pragma unroll
@@ -1250,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   TC_MARK(tid == 0, 8);
-  if (warp >= kFirstProducer) cluster_wait();  // pairs with the arrival after set-up
+  if (is_producer || is_mma) cluster_wait();  // pairs with the arrival after set-up
   // this CTA's outputs are issued: the merge kernel (launched as a dependent
   // grid) may start its set-up; it waits for this grid's completion before
   // reading any partial

@@ -1145,26 +1145,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx4[c & 3] = fmaxf(mx4[c & 3], v);
         }
         const float mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        // The row's maximum is needed only when it moves the running max:
-        // one barrier tells whether any quarter row of these 32 rows wants
-        // that (its own maximum beyond m + kRescale); only then are the
-        // quarter maxima exchanged. Either way a row rescales exactly when
-        // its maximum exceeds m + kRescale.
+        float* mrow = mxs + (b * kOwnRows + ro) * kRowThreads;
+        mrow[h] = mxh;
+        named_bar_sync(quad_bar, 128);
+        TC_TRACE(arms, TR_SOFTMAX, g, 2);
+        const float4 m4 = *reinterpret_cast<const float4*>(mrow);
+        const float mb = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
         float corr = 1.f;
         bool resc = false;
-        if (named_bar_or(quad_bar, 128, mxh > m + kRescale)) {
-          float* mrow = mxs + (b * kOwnRows + ro) * kRowThreads;
-          mrow[h] = mxh;
-          named_bar_sync(quad_bar, 128);
-          const float4 m4 = *reinterpret_cast<const float4*>(mrow);
-          const float mb = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
-          if (mb > m + kRescale) {
-            corr = ex2_approx(m - mb);
-            m = mb;
-            resc = true;
-          }
+        if (mb > m + kRescale) {
+          corr = ex2_approx(m - mb);
+          m = mb;
+          resc = true;
         }
-        TC_TRACE(arms, TR_SOFTMAX, g, 2);
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[kQCols / 2];
         if (m == -INFINITY) {

@@ -51,7 +51,7 @@ typedef uint16_t mt_bf16;                  /* raw bf16 bits */
 enum {
   MT_OK = 0,
   MT_EINVAL = -1,        /* bad pointer, size, alignment or scalar */
-  MT_EUNSUPPORTED = -2,  /* valid request this build cannot serve */
+  MT_EUNSUPPORTED = -2,  /* valid request the library cannot serve */
   MT_EWORKSPACE = -3,    /* workspace missing, misaligned or too small */
   MT_ECUDA = -4,         /* a CUDA runtime call or launch failed */
   MT_ESCRATCH = -5       /* needs more scratch than mla_tree_verify_noalloc's

@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    mbar_init(&bars[B_QT_FULL], kSoftThreads + 64);   // softmax threads + senders
+    mbar_init(&bars[B_QT_FULL], kSoftThreads / 32 + 2);  // softmax and sender warps
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int s = 0; s < kStages; ++s) {
       for (int w = 0; w < kProducers; ++w) mbar_init(&bars[B_KV_FULL0 + s * kProducers + w], 1);
@@ -427,17 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[B_S_FULL0 + s], 1);
-      mbar_init(&bars[B_S_EMPTY0 + s], kSoftThreads + 64);  // softmax threads + senders
+      mbar_init(&bars[B_S_EMPTY0 + s], kSoftThreads / 32 + 2);  // softmax and sender warps
       mbar_init(&bars[B_SX_FULL0 + s], 1);            // armed once per block, + the peer's bytes
       mbar_init(&bars[B_SX_FREE0 + s], kSoftThreads / 32);  // the peer's softmax warps
       mbar_init(&bars[B_PX_FULL0 + s], 1);
       mbar_init(&bars[B_PX_FREE0 + s], 2);            // the peer's two receiver warps
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[B_P_FULL0 + s], kSoftThreads + 64);  // softmax threads + receivers
+      mbar_init(&bars[B_P_FULL0 + s], kSoftThreads / 32 + 2);  // softmax and receiver warps
       mbar_init(&bars[B_O_DONE0 + s], 1);
     }
-    mbar_init(&bars[B_O_FREE], kSoftThreads + 64);
+    mbar_init(&bars[B_O_FREE], kSoftThreads / 32 + 2);  // softmax and receiver warps
     mbar_init(&bars[B_DRAIN], 1);
     *abort = 0;
     fence_mbar_init_cluster();
@@ -769,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_QT_FULL]);
+        __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+        if (lane == 0) mbar_arrive(&bars[B_QT_FULL]);
       }
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
@@ -784,7 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_regs_ready(s0);
         tmem_regs_ready(s1);
         tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
+        __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+        if (lane == 0) mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
         float x[BN];
 #pragma unroll
         for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]) * scale2;
@@ -880,7 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
+        __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+        if (lane == 0) mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
         TC_TRACE(arms, TR_RECEIVER, g, 2);
       }
       // epilogue: this CTA's 256 value dims of the row, divided by the
@@ -920,7 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
+      __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+      if (lane == 0) mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
       TC_MARK(arms, 7);
     }
   } else {
@@ -978,7 +982,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[B_QT_FULL]);
+      __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+      if (lane == 0) mbar_arrive(&bars[B_QT_FULL]);
     };
 
     int id = item_of(0, cluster_id, p.nclusters);
@@ -1114,7 +1119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY0 + b]);
+        __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+        if (lane == 0) mbar_arrive(&bars[B_S_EMPTY0 + b]);
         // the peer's partials of the same columns (already in the log2 domain)
         if (!dead) dead = !mbar_wait<true>(&bars[B_SX_FULL0 + b], ph, abort, limit);
         TC_TRACE(arms, TR_SOFTMAX, g, 1);
@@ -1237,7 +1243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
+        __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+        if (lane == 0) mbar_arrive(&bars[B_P_FULL0 + (g & 1)]);
         TC_TRACE(arms, TR_SOFTMAX, g, 5);
       }
 
@@ -1287,7 +1294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         else a.ws_lse[(int64_t)it.split * R + grow] = lv;
       }
       tc_fence_before();
-      mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
+      __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
+      if (lane == 0) mbar_arrive(&bars[B_O_FREE]);  // O has been read: the next item may overwrite it
       TC_MARK(arms, 6);
     }
   }

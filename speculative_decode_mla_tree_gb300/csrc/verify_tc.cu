@@ -21,9 +21,10 @@
 //             per instruction, several stages in flight
 //   tcgen05   S_c = Q_c K_c^T   (M=128, N=48, K=288) into TMEM
 //   DSMEM     each CTA sends its fp32 partial scores of the rows the other
-//             CTA owns (64 rows x 48) to that CTA
+//             CTA owns (64 rows x 48) to that CTA; with the byte-form mask
+//             the senders apply the mask (a hidden column is sent as -inf)
 //   softmax   the owner adds the two fp32 partials (exact scores of its
-//             rows, in the log2 domain), applies the tree mask and runs the
+//             rows, in the log2 domain), applies the bit-form mask and runs the
 //             online softmax (four threads per row, 12 columns each; lazy
 //             rescaling: the running max moves only when it grows by more
 //             than 8, i.e. a factor of 256); it writes its rows of P (bf16)
@@ -43,10 +44,10 @@
 // scheduler are warp % 4): in CTA c the eight warps whose quarter holds the
 // own rows run the softmax (four threads per row) and the own rows'
 // epilogue, so the own rows' two schedulers run nothing else. On the other
-// two schedulers, warps 0-3 send partial scores, warps 4-7 receive P and run
-// those rows' epilogue, and of warps 8-15 one issues the MMAs and owns TMEM
-// while three are TMA producers (one warp alone issues tile::gather4 too
-// slowly to keep up). Every mbarrier wait is time-bounded: a timeout sets
+// two schedulers, warps 0-3 send partial scores (and apply a byte-form
+// mask), warps 4-7 receive P and run those rows' epilogue, and of warps
+// 8-15 one issues the MMAs and owns TMEM while three are TMA producers (one
+// warp alone issues tile::gather4 too slowly to keep up). Every mbarrier wait is time-bounded: a timeout sets
 // MT_DEV_TIMEOUT, after which no thread issues another copy, MMA or remote
 // store, every loop runs to its end (so no named barrier is left waiting)
 // and the copies and MMAs in flight are drained before TMEM is released.
@@ -710,8 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Thread rp owns tile row 64 (1 - c) + rp, which the peer's softmax
     // runs. Per item it writes that row's latent query half into TMEM (QK's
     // A operand); per block it reads the row's fp32 partial score from TMEM,
-    // scales it into the log2 domain and stores it into the peer's SX
-    // buffer, whose arrival completes the peer's SX_FULL.
+    // scales it into the log2 domain (-inf for a column the byte-form mask
+    // hides) and stores it into the peer's SX buffer, whose arrival
+    // completes the peer's SX_FULL.
     const int rp = (q4 - 2 * (int)(1u - cta)) * 32 + lane;
     const int r = 64 * (int)(1u - cta) + rp;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
@@ -772,8 +774,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // one arrival per warp: the warp's TMEM accesses are collective
         if (lane == 0) mbar_arrive(&bars[B_QT_FULL]);
       }
+      // Byte-form mask (the bit form is applied by the owner's softmax): the
+      // bytes of a block arrive as (draft node, 8-column group) pairs over
+      // the nodes of the peer's rows; sender thread rp owns pairs rp + 64 k,
+      // held one block ahead when they are few enough. Row r's hidden
+      // columns are sent as -inf.
+      const int rows_req = it.n * H;
+      const int node = (it.row0 + r < rows_req ? it.row0 + r : rows_req - 1) / H;
+      const int pre = kSkip ? it.L - it.n : 0;  // prefix columns: visible, mask unread
+      const int peer0 = it.row0 + 64 * (int)(1u - cta);
+      const int i_lo = min(peer0, rows_req - 1) / H;
+      const int cnt = max(1, min(it.n - 1, (peer0 + kOwnRows - 1) / H) - i_lo + 1);
+      constexpr int kGroups = BN / 8;  // 8-column groups per block row
+      const int pairs = cnt * kGroups;
+      const bool prefetch = pairs <= kOwnRows * kMaskPrefetch;
+      uint8_t raw[kMaskPrefetch][8];
+      auto load_mask = [&](int blk_) {
+        const int jb_ = it.j0 + blk_ * BN;
+#pragma unroll
+        for (int k = 0; k < kMaskPrefetch; ++k) {
+          const int q = rp + kOwnRows * k;
+          if (q < pairs) {
+            const int pos0 = jb_ + 8 * (q % kGroups);
+            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              raw[k][e] = pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) ? __ldg(src + e) : 0;
+          }
+        }
+      };
+      if (!kBits && prefetch) load_mask(0);
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
+        uint64_t vm = ~0ull;
+        if constexpr (!kBits) {
+          const int jb = it.j0 + blk * BN;
+          uint8_t* vb = reinterpret_cast<uint8_t*>(vis + b * kVisNodes);
+          if (prefetch) {
+#pragma unroll
+            for (int k = 0; k < kMaskPrefetch; ++k) {
+              const int q = rp + kOwnRows * k;
+              if (q < pairs) {
+                uint32_t bits = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
+                vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
+              }
+            }
+            if (blk + 1 < it.nblocks) load_mask(blk + 1);
+          } else {
+            for (int q = rp; q < pairs; q += kOwnRows) {
+              const int pos0 = jb + 8 * (q % kGroups);
+              const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
+              uint32_t bits = 0;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) && __ldg(src + e)) bits |= 1u << e;
+              vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
+            }
+          }
+          named_bar_sync(3, kOwnRows);  // the two sender warps
+          const int ni = node - i_lo;
+          vm = (ni >= 0 && ni < cnt) ? vis[b * kVisNodes + ni] : 0ull;
+          if (kSkip && pre > jb) {  // the block's prefix columns, up to the split's end
+            const int pc = min(pre, it.j1) - jb;
+            vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
+          }
+        }
         if (!dead) dead = !mbar_wait<false>(&bars[B_S_FULL0 + b], ph, abort, limit);
         TC_TRACE(tr, TR_SENDER, g, 0);
         tc_fence_after();
@@ -789,7 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[B_S_EMPTY0 + b]);  // the score buffer may take block g+2
         float x[BN];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]) * scale2;
+        for (int c = 0; c < BN; ++c)
+          x[c] = (vm >> c) & 1ull ? __uint_as_float(c < 32 ? s0[c] : s1[c - 32]) * scale2 : -INFINITY;
         // the peer's softmax has read block g-2 from this buffer
         if (!dead) dead = !mbar_wait<false>(&bars[B_SX_FREE0 + b], ph ^ 1, abort, limit);
         if (!dead && !*abort) {
@@ -937,7 +1005,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = wg;
     const int ro = (q4 - 2 * (int)cta) * 32 + lane;
     const int r = 64 * (int)cta + ro;
-    const int st_idx = 64 * h + ro;                  // 0..255 over the softmax threads
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t t_o = tmem + lane_base + kTmemO + 64 * h;
     const uint32_t sxfree_peer0 = mapa(smem_u32(&bars[B_SX_FREE0]), peer);
@@ -995,35 +1062,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < rows_req;
       const int node = (valid ? row : rows_req - 1) / H;
       const int pre = kSkip ? it.L - it.n : 0;  // prefix columns: visible, mask unread
-      // Byte mask: the bits of a block arrive as (draft node, 8-column
-      // group) pairs over the nodes of the own rows; softmax thread st_idx
-      // owns pairs st_idx + 256 k. When the own rows touch few enough nodes
-      // (every case with 4 or more heads), the bytes of block blk+1 are
-      // loaded while block blk is processed.
-      const int own0 = min(it.row0 + 64 * (int)cta, rows_req - 1);
-      const int i_lo = own0 / H;
-      const int i_hi = min(it.n - 1, (it.row0 + 64 * (int)cta + kOwnRows - 1) / H);
-      const int cnt = max(1, i_hi - i_lo + 1);
-      constexpr int kGroups = BN / 8;  // 8-column groups per block row
-      const int pairs = cnt * kGroups;
-      const bool prefetch = pairs <= kSoftThreads * kMaskPrefetch;
-      uint8_t raw[kMaskPrefetch][8];
-      auto load_mask = [&](int blk_) {
-        const int jb_ = it.j0 + blk_ * BN;
-#pragma unroll
-        for (int k = 0; k < kMaskPrefetch; ++k) {
-          const int q = st_idx + kSoftThreads * k;
-          if (q < pairs) {
-            const int pos0 = jb_ + 8 * (q % kGroups);
-            const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              raw[k][e] = pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) ? __ldg(src + e) : 0;
-          }
-        }
-      };
       // Bit-form mask: this row's node reads the (up to) three words holding
       // a block's 48 columns straight from global memory, one block ahead.
+      // (With the byte form the score senders apply the mask: hidden columns
+      // arrive as -inf in the peer's partial scores.)
       const int mw = (it.L + 31) >> 5;
       const uint32_t* mrow = kBits ? a.mask_bits + it.mask0 + (int64_t)node * mw : nullptr;
       uint32_t mnext[3] = {0u, 0u, 0u};
@@ -1034,56 +1076,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           mnext[k] = wi + k < mw && (!kSkip || 32 * (wi + k) + 32 > pre) ? __ldg(mrow + wi + k) : 0u;
       };
       if (kBits) load_bits(0);
-      else if (prefetch) load_mask(0);
       float m = -INFINITY, lh = 0.f;
       for (int blk = 0; blk < it.nblocks; ++blk, ++g) {
         const uint32_t b = g & 1, ph = (g >> 1) & 1;
         const int jb = it.j0 + blk * BN;
         TC_TRACE(arms, TR_SOFTMAX, g, 8);
-        uint64_t vm;
-        if (kBits) {
+        uint32_t vh = 0;  // visibility of the thread's 12 columns (bit form)
+        if constexpr (kBits) {
           const uint32_t w0 = mnext[0], w1 = mnext[1], w2 = mnext[2];
           if (blk + 1 < it.nblocks) load_bits(blk + 1);
           const int o = jb & 31;
           const uint64_t lo = (uint64_t)w0 | ((uint64_t)w1 << 32);
-          vm = o ? (lo >> o) | ((uint64_t)w2 << (64 - o)) : lo;
+          uint64_t vm = o ? (lo >> o) | ((uint64_t)w2 << (64 - o)) : lo;
           const int lim = it.j1 - jb;  // columns of this block inside the split
           if (lim < 64) vm &= (1ull << lim) - 1ull;
-        } else {
-          // visibility bits of this block for the own rows' draft nodes
-          uint8_t* vb = reinterpret_cast<uint8_t*>(vis + b * kVisNodes);
-          if (prefetch) {
-#pragma unroll
-            for (int k = 0; k < kMaskPrefetch; ++k) {
-              const int q = st_idx + kSoftThreads * k;
-              if (q < pairs) {
-                uint32_t bits = 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) bits |= (raw[k][e] != 0 ? 1u : 0u) << e;
-                vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
-              }
-            }
-            if (blk + 1 < it.nblocks) load_mask(blk + 1);
-          } else {
-            for (int q = st_idx; q < pairs; q += kSoftThreads) {
-              const int pos0 = jb + 8 * (q % kGroups);
-              const uint8_t* src = a.mask + it.mask0 + (int64_t)(i_lo + q / kGroups) * it.L + pos0;
-              uint32_t bits = 0;
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (pos0 + e < it.j1 && (!kSkip || pos0 + e >= pre) && __ldg(src + e)) bits |= 1u << e;
-              vb[(q / kGroups) * 8 + q % kGroups] = (uint8_t)bits;
-            }
+          if (kSkip && pre > jb) {  // the block's prefix columns, up to the split's end
+            const int pc = min(pre, it.j1) - jb;
+            vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
           }
-          named_bar_sync(3, kSoftThreads);
-          const int ni = node - i_lo;
-          vm = (ni >= 0 && ni < cnt) ? vis[b * kVisNodes + ni] : 0ull;
+          vh = (uint32_t)(vm >> (kQCols * h)) & ((1u << kQCols) - 1u);
         }
-        if (kSkip && pre > jb) {  // the block's prefix columns, up to the split's end
-          const int pc = min(pre, it.j1) - jb;
-          vm |= pc >= 64 ? ~0ull : (1ull << pc) - 1ull;
-        }
-        const uint32_t vh = (uint32_t)(vm >> (kQCols * h)) & ((1u << kQCols) - 1u);
         TC_TRACE(arms, TR_SOFTMAX, g, 9);
 
         // this CTA's partial scores of the row's 12 columns, from TMEM
@@ -1146,9 +1158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kQCols; ++c) {
-          const float v = (vh >> c) & 1u ? s[c] : -INFINITY;
-          s[c] = v;
-          mx4[c & 3] = fmaxf(mx4[c & 3], v);
+          if constexpr (kBits) s[c] = (vh >> c) & 1u ? s[c] : -INFINITY;
+          mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
         }
         const float mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         float* mrow = mxs + (b * kOwnRows + ro) * kRowThreads;

@@ -116,11 +116,6 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
            : a.bits_mask ? ((__ldg(a.mask_bits + mrow0 + (j >> 5)) >> (j & 31)) & 1u) != 0
                          : __ldg(a.mask + mrow0 + j) != 0;
   };
-  auto usable = [&](int32_t slot) -> bool {
-    if (slot >= 0 && slot < a.num_slots) return true;
-    if (lane == 0) flag(a.status, MT_DEV_BAD_SLOT);
-    return false;
-  };
   // one key of row r: its score and the online-softmax update
   auto update = [&](int r, const float (&kf)[18]) {
     float d = 0.f;
@@ -140,18 +135,33 @@ __global__ void __launch_bounds__(kWarps * 32) verify_simt_kernel(const VerifyAr
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc[r][e] = fmaf(p, kf[e], acc[r][e]);
   };
-  for (int j = wj0; j < wj1; j += 2) {
-    const bool two = j + 1 < wj1;
-    const int32_t s0 = __ldg(idx + j), s1 = two ? __ldg(idx + j + 1) : 0;
-    const bool v0 = usable(s0) && visible(j);
-    const bool v1 = two && usable(s1) && visible(j + 1);
-    float k0[18], k1[18];
-    if (v0) load_row18(a.kv + (int64_t)s0 * kDqk, lane, 1.f, k0);
-    if (v1) load_row18(a.kv + (int64_t)s1 * kDqk, lane, 1.f, k1);
+  // The piece goes in batches of 32 keys: lane i reads key i's slot and
+  // visibility first (one round of loads for the batch; a bad slot is
+  // flagged and skipped), then the keys are taken two at a time, so the
+  // only loads left in the key loop are the rows themselves.
+  for (int jb = wj0; jb < wj1; jb += 32) {
+    const int nb = min(32, wj1 - jb);
+    int32_t my_slot = 0;
+    bool my_vis = false;
+    if (lane < nb) {
+      my_slot = __ldg(idx + jb + lane);
+      const bool ok = my_slot >= 0 && my_slot < a.num_slots;
+      if (!ok) flag(a.status, MT_DEV_BAD_SLOT);
+      my_vis = ok && visible(jb + lane);
+    }
+    const uint32_t vis = __ballot_sync(0xffffffffu, my_vis);
+    for (int i = 0; i < nb; i += 2) {
+      const int32_t s0 = __shfl_sync(0xffffffffu, my_slot, i);
+      const int32_t s1 = __shfl_sync(0xffffffffu, my_slot, (i + 1) & 31);
+      const bool v0 = (vis >> i) & 1u, v1 = i + 1 < nb && ((vis >> (i + 1)) & 1u);
+      float k0[18], k1[18];
+      if (v0) load_row18(a.kv + (int64_t)s0 * kDqk, lane, 1.f, k0);
+      if (v1) load_row18(a.kv + (int64_t)s1 * kDqk, lane, 1.f, k1);
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      if (v0) update(r, k0);
-      if (v1) update(r, k1);
+      for (int r = 0; r < kRows; ++r) {
+        if (v0) update(r, k0);
+        if (v1) update(r, k1);
+      }
     }
   }
 
@@ -225,8 +235,14 @@ cudaError_t launch_verify_simt(const VerifyArgs& a, int num_sms, cudaStream_t st
   });
   if (g_simt_attr != cudaSuccess) return g_simt_attr;
   const int hg_count = (a.heads + kRows - 1) / kRows;
+  // No request has more keys than kv_indices holds, and a split holds at
+  // least kMinKeysY keys, so no request uses more than this many splits:
+  // CTAs beyond it would only find that out (after reading the request's
+  // geometry) and exit.
+  const int64_t need = (a.kv_len + kMinKeysY - 1) / kMinKeysY;
+  const int gy = (int)(need < 1 ? 1 : need < a.max_splits ? need : a.max_splits);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)a.total_q * hg_count), (unsigned)a.max_splits);
+  cfg.gridDim = dim3((unsigned)((int64_t)a.total_q * hg_count), (unsigned)gy);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = kSimtSmem;
   cfg.stream = stream;

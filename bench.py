@@ -141,12 +141,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+def _code_tokens(text):
+    """C/CUDA source with its comments removed and every run of white space
+    outside string and character literals made one space, so that editing a
+    comment or the layout does not change what is hashed."""
+    out, i, n = [], 0, len(text)
+
+    def space():
+        if out and out[-1] != " ":
+            out.append(" ")
+
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            space()
+        elif c.isspace():
+            space()
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out).strip()
+
+
 def _kernel_source_hash():
+    """Hash of the kernel sources the DRAM traffic in profiles/traffic.json
+    was measured on (code only: see _code_tokens)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decode_mla_tree_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("verify") or name.endswith((".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(_code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

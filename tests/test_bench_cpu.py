@@ -6,7 +6,8 @@
 * The algorithmic bytes are recomputed from their definition for both mask
   forms and the prefix skip.
 * The committed DRAM traffic is reported only while the kernel sources it
-  was measured on are unchanged."""
+  was measured on are unchanged; comments and layout do not count as a
+  change, code does."""
 import importlib.util
 import json
 import os
@@ -82,3 +83,16 @@ def test_committed_traffic_names_its_sources(bench):
         assert key.startswith("verify_c")
         assert e["dram_bytes_per_launch"] > 0
         assert len(e["source_hash"]) == 16
+
+
+def test_source_hash_ignores_comments_not_code(bench):
+    base = 'int f(int x) {\n  return x + 1;  // one more\n}\nconst char* s = "a // b /* c */";\n'
+    same = ('/* header\n   text */\nint f(int x)\n{\n    return x + 1;\n}\n'
+            'const char* s = "a // b /* c */";  // the string keeps its slashes\n')
+    other = 'int f(int x) {\n  return x + 2;  // one more\n}\nconst char* s = "a // b /* c */";\n'
+    lit = 'int f(int x) {\n  return x + 1;  // one more\n}\nconst char* s = "a //  b /* c */";\n'
+    t = bench._code_tokens
+    assert t(base) == t(same)
+    assert t(base) != t(other)
+    assert t(base) != t(lit)      # white space inside a literal is code
+    assert "one more" not in t(base) and "// b /* c */" in t(base)

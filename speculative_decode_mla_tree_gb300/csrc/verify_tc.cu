@@ -36,9 +36,11 @@
 //
 // Why two CTAs: a 128-row fp32 accumulator for all 512 value dims is the
 // whole 256 KB of TMEM. Splitting the dims halves it and leaves TMEM room
-// for the query's latent half (so the QK MMAs read no query bytes from
-// shared memory) and two score buffers. The scores cross between the CTAs
-// in fp32, so no partial is rounded below fp32 before the softmax.
+// for 224 of the query half's 256 latent dims (14 of a block's 18 QK MMAs
+// take the query from TMEM; the last 32 latent dims and the rope half come
+// from shared memory), two score buffers and two P buffers. The scores cross
+// between the CTAs in fp32, so no partial is rounded below fp32 before the
+// softmax.
 //
 // Roles per CTA (512 threads, 16 warps; a warp's TMEM lane quarter and its
 // scheduler are warp % 4): in CTA c the eight warps whose quarter holds the
@@ -79,7 +81,7 @@ static_assert(kProducers == 3, "warps 8-15 of the two non-softmax quarters: one 
 constexpr int kMaxBatch = 256;   // requests per launch (the plan lives in shared memory)
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int kMinChunk = 256;   // smallest split worth a work item (key rows)
-constexpr int kMaskPrefetch = 2; // mask (node, group) pairs per thread held one block ahead
+constexpr int kMaskPrefetch = 2; // byte-mask (node, group) pairs per score-sender thread held one block ahead
 constexpr int kSlotAhead = 2;    // key blocks whose slot numbers are in flight ahead of the gathers
 constexpr int kGroupsPerWarp = kGatherLanes / kProducers;
 static_assert(kGatherLanes % kProducers == 0, "groups per producer warp");

@@ -46,12 +46,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-// Arrive (release at cluster scope) on a barrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
-}
-
 // Arrive without release semantics on a barrier of another CTA: for signals
 // whose guarded accesses are already complete (e.g. loads whose values have
 // been consumed), which spares the cluster-scope fence of a release.
@@ -214,34 +208,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// The same two with the accumulate flag fixed at compile time (no
-// predicate to compute per instruction).
-template <int kAcc>
-__device__ __forceinline__ void mma_bf16_ss_c(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(kAcc)
-      : "memory");
-}
-template <int kAcc>
-__device__ __forceinline__ void mma_bf16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                              uint32_t idesc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kAcc)
-      : "memory");
-}
-
-// A shared-memory descriptor moved by `bytes` (a multiple of 16): the start
-// address is the low 14-bit field in 16-byte units, and shared-memory
-// addresses stay below 256 KB, so the add never carries out of the field.
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
-  return desc + (uint64_t)(bytes >> 4);
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -274,38 +240,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
       :
       : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-        "+r"(r[14]), "+r"(r[15])
-      :
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7])
-               :
-               : "memory");
 }
 
 // The same loads without their wait, to overlap several: the registers are
@@ -458,13 +392,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t remote_addr, uint32_t a, ui
       "r"(a), "r"(b), "r"(remote_bar)
       : "memory");
 }
-__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t a, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
-      "r"(a), "r"(remote_bar)
-      : "memory");
-}
-
 // 2^x on the special-function unit (about 2 ulp; denormal results flush to 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -472,10 +399,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// generic-proxy writes to shared memory become visible to the async proxy
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

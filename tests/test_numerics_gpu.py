@@ -5,8 +5,8 @@ workloads the way a serving engine runs them, against the fp64 oracle.
   half-dot-products that are large and cancel exactly, and values beyond the
   fp16 range. Every factor is a power of two, so the inputs are exact in
   bf16 and the oracle's expectations need no other reasoning. Both kernels,
-  unsplit and split (the split partials and their merge are where a narrow
-  intermediate format would overflow or round). These inputs push single
+  both mask forms, unsplit and split (the split partials and their merge are
+  where a narrow intermediate format would overflow or round). These inputs push single
   outputs to magnitudes of 4-5, so the comparison adds the bf16 rounding of
   the output itself (2^-9 |ref|) to the stated bounds.
 * The 64-request ragged workload (prefixes 128..131072, 8..64-node trees,
@@ -50,12 +50,16 @@ def _ref(kind):
     return _refs[kind]
 
 
+@pytest.mark.parametrize("bits", [True, False], ids=["bits", "bytes"])
 @pytest.mark.parametrize("splits", [0, 7], ids=["auto", "split7"])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("kind", W.STRESS_KINDS)
-def test_stress_inputs(kind, path, splits):
+def test_stress_inputs(kind, path, splits, bits):
+    """Both mask forms: the tensor-core kernel applies the bit form in the
+    softmax and the byte form in the score exchange (hidden columns sent as
+    -inf), so each form meets the stress inputs on its own code."""
     w, (out, lse) = _ref(kind)
-    st = VerifyStep(w, path=path, max_splits=splits, mask_bits=True)
+    st = VerifyStep(w, path=path, max_splits=splits, mask_bits=bits)
     st.run()
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0

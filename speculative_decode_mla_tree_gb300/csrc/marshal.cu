@@ -345,7 +345,7 @@ __device__ __forceinline__ void mask_bits_body(
     const int32_t* __restrict__ kptr, const int32_t* __restrict__ pptr, int batch, int total_q,
     int64_t* __restrict__ word_indptr, uint32_t* __restrict__ words, int64_t capacity,
     int32_t* status, int b, int g, int groups) {
-  __shared__ uint32_t bits[MT_MAX_TREE / 32];
+  __shared__ uint32_t bits[kMaskThreads / 32][MT_MAX_TREE / 32];  // one ancestor bitset per warp
   long long s_base, s_bad;
   mask_offsets(
       qptr, batch, b,
@@ -372,20 +372,26 @@ __device__ __forceinline__ void mask_bits_body(
   // the request's parent array, staged once (the walks below would otherwise
   // be a chain of dependent global loads, one per tree level)
   __shared__ int16_t par_s[MT_MAX_TREE];
-  if (g < n) {
-    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
-      const int32_t p = parents[q0 + k];
-      par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);  // -2: out of range
-    }
+  constexpr int kWarpsM = kMaskThreads / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if ((int64_t)g * kWarpsM >= n) return;  // no row of this request falls to this block
+  for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
+    const int32_t p = parents[q0 + k];
+    par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);  // -2: out of range
   }
-  for (int64_t i = g; i < n; i += groups) {
-    for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
-    __syncthreads();
-    if (threadIdx.x == 0) {
+  __syncthreads();
+  // One row per warp at a time (rows g * 8 + warp, stepping by 8 * groups),
+  // with the row's ancestor set in the warp's own slice of `bits`, so no
+  // row waits for the block.
+  uint32_t* wbits = bits[wid];
+  for (int64_t i = (int64_t)g * kWarpsM + wid; i < n; i += (int64_t)groups * kWarpsM) {
+    for (int w = lane; w < nwords; w += 32) wbits[w] = 0u;
+    __syncwarp();
+    if (lane == 0) {
       // Ancestor-or-self walk; parents strictly decrease, so at most n steps.
       int64_t k = i;
       while (k >= 0) {
-        bits[k >> 5] |= 1u << (k & 31);
+        wbits[k >> 5] |= 1u << (k & 31);
         const int p = par_s[k];
         if (p == -2) {
           flag(status, MT_DEV_BAD_PARENT);
@@ -394,9 +400,9 @@ __device__ __forceinline__ void mask_bits_body(
         k = p;
       }
     }
-    __syncthreads();
+    __syncwarp();
     uint32_t* row = words + base + i * W;
-    for (int64_t w = threadIdx.x; w < W; w += blockDim.x) {
+    for (int64_t w = lane; w < W; w += 32) {
       const int64_t c0 = w << 5;
       uint32_t v;
       if (c0 + 32 <= P) {
@@ -408,13 +414,13 @@ __device__ __forceinline__ void mask_bits_body(
           const int64_t col = c0 + e;
           uint32_t on = 0;
           if (col < P) on = 1;
-          else if (col < L) on = (bits[(col - P) >> 5] >> ((col - P) & 31)) & 1u;
+          else if (col < L) on = (wbits[(col - P) >> 5] >> ((col - P) & 31)) & 1u;
           v |= on << e;
         }
       }
       row[w] = v;
     }
-    __syncthreads();
+    __syncwarp();
   }
 }
 

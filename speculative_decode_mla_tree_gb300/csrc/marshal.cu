@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
     const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
     const int32_t* __restrict__ kptr, int batch, int total_q, int64_t* __restrict__ mask_indptr,
     uint8_t* __restrict__ mask, int64_t capacity, int32_t* status) {
-  __shared__ uint32_t bits[MT_MAX_TREE / 32];
+  __shared__ uint32_t bits[kMaskThreads / 32][MT_MAX_TREE / 32];  // one ancestor bitset per warp
   const int b = blockIdx.y;
   long long s_base, s_bad;
   mask_offsets(
@@ -252,20 +252,26 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
   const int words = (int)((n + 31) >> 5);
   // the request's parent array, staged once (-2: out of range)
   __shared__ int16_t par_s[MT_MAX_TREE];
-  if (blockIdx.x < n) {
-    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
-      const int32_t p = parents[q0 + k];
-      par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);
-    }
+  constexpr int kWarpsM = kMaskThreads / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if ((int64_t)blockIdx.x * kWarpsM >= n) return;  // no row of this request falls to this block
+  for (int64_t k = threadIdx.x; k < n; k += blockDim.x) {
+    const int32_t p = parents[q0 + k];
+    par_s[k] = (int16_t)(p < -1 || p >= k ? -2 : p);
   }
-  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
-    for (int w = threadIdx.x; w < words; w += blockDim.x) bits[w] = 0u;
-    __syncthreads();
-    if (threadIdx.x == 0) {
+  __syncthreads();
+  // One row per warp at a time (rows blockIdx.x * 8 + warp, stepping by
+  // 8 * gridDim.x), the row's ancestor set in the warp's own bitset, so no
+  // row waits for the block.
+  uint32_t* wbits = bits[wid];
+  for (int64_t i = (int64_t)blockIdx.x * kWarpsM + wid; i < n; i += (int64_t)gridDim.x * kWarpsM) {
+    for (int w = lane; w < words; w += 32) wbits[w] = 0u;
+    __syncwarp();
+    if (lane == 0) {
       // Ancestor-or-self walk; parents strictly decrease, so at most n steps.
       int64_t k = i;
       while (k >= 0) {
-        bits[k >> 5] |= 1u << (k & 31);
+        wbits[k >> 5] |= 1u << (k & 31);
         const int p = par_s[k];
         if (p == -2) {
           flag(status, MT_DEV_BAD_PARENT);
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
         k = p;
       }
     }
-    __syncthreads();
+    __syncwarp();
     uint8_t* row = mask + base + i * L;
     const uintptr_t a = (uintptr_t)row, e = a + (uintptr_t)L;
     uintptr_t a0 = (a + 15) & ~(uintptr_t)15;
@@ -283,13 +289,13 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
     if (a1 < a0) a1 = a0;
     // head and tail bytes
     const int64_t head = (int64_t)(a0 - a), tail = (int64_t)(e - a1);
-    for (int64_t c = threadIdx.x; c < head + tail; c += blockDim.x) {
+    for (int64_t c = lane; c < head + tail; c += 32) {
       const int64_t col = c < head ? c : (int64_t)(a1 - a) + (c - head);
-      row[col] = mask_byte(col, P, bits);
+      row[col] = mask_byte(col, P, wbits);
     }
     // interior 16-byte chunks
     const int64_t chunks = (int64_t)(a1 - a0) >> 4;
-    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+    for (int64_t c = lane; c < chunks; c += 32) {
       const int64_t col0 = (int64_t)(a0 - a) + (c << 4);
       uint4 v;
       if (col0 + 16 <= P) {
@@ -300,14 +306,14 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_pack_kernel(
         for (int q = 0; q < 4; ++q) {
           uint32_t x = 0;
 #pragma unroll
-          for (int y = 0; y < 4; ++y) x |= (uint32_t)mask_byte(col0 + q * 4 + y, P, bits) << (8 * y);
+          for (int y = 0; y < 4; ++y) x |= (uint32_t)mask_byte(col0 + q * 4 + y, P, wbits) << (8 * y);
           w[q] = x;
         }
         v = make_uint4(w[0], w[1], w[2], w[3]);
       }
       *(uint4*)(row + col0) = v;
     }
-    __syncthreads();
+    __syncwarp();
   }
 }
 

@@ -207,13 +207,14 @@ __device__ __forceinline__ void mask_offsets(const int32_t* __restrict__ qptr, i
   }
 }
 
-// grid (row groups, batch). Each CTA: compute its request's mask offset by
-// summing n*L over earlier requests (all threads loading at once); for each
-// of its rows, walk the parent
-// chain once into a shared bitset, then write the row: prefix bytes 1, draft
-// byte k = bit k. Interior 16-byte chunks go out as one vector store; the
-// head and tail bytes of a row (which may share a 16-byte chunk with the
-// neighbouring row) are written byte by byte so no byte has two writers.
+// grid (row groups, batch). Each CTA computes its request's mask offset by
+// summing n*L over earlier requests (all threads loading at once) and stages
+// the request's parents in shared memory. Each warp then takes one of the
+// CTA's rows at a time: it walks the row's parent chain once into its own
+// bitset and writes the row: prefix bytes 1, draft byte k = bit k. Interior
+// 16-byte chunks go out as one vector store; the head and tail bytes of a
+// row (which may share a 16-byte chunk with the neighbouring row) are
+// written byte by byte so no byte has two writers.
 constexpr int kMaskThreads = 256;
 
 __device__ __forceinline__ uint8_t mask_byte(int64_t col, int64_t P, const uint32_t* bits) {
@@ -345,7 +346,7 @@ __device__ __forceinline__ long long req_len(const int32_t* kptr, const int32_t*
   return ((long long)pptr[r + 1] - pptr[r]) + ((long long)qptr[r + 1] - qptr[r]);
 }
 
-// Row group g (of `groups`, kMaskThreads threads each) of request b.
+// Row group g (of `groups`, kMaskThreads threads each, one row per warp at a time) of request b.
 __device__ __forceinline__ void mask_bits_body(
     const int32_t* __restrict__ parents, const int32_t* __restrict__ qptr,
     const int32_t* __restrict__ kptr, const int32_t* __restrict__ pptr, int batch, int total_q,

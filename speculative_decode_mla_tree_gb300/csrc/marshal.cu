@@ -106,8 +106,24 @@ __device__ __forceinline__ void indices_body(
     return;
   }
   const int64_t L = P + n;
-  for (int64_t j = (int64_t)c * 256 + threadIdx.x; j < L; j += (int64_t)chunks * 256)
-    kv_indices[base + j] = j < P ? pidx[p0 + j] : loc[q0 + (j - P)];
+  // Thread t of chunk c copies elements c * 256 + t + k * step. Eight of
+  // them are loaded before any is stored, so eight loads are in flight at
+  // once: a long prefix is otherwise a chain of one memory latency per 256 x
+  // chunks elements.
+  const int64_t step = (int64_t)chunks * 256;
+  for (int64_t j0 = (int64_t)c * 256 + threadIdx.x; j0 < L; j0 += 8 * step) {
+    int32_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + u * step;
+      v[u] = j < L ? (j < P ? pidx[p0 + j] : loc[q0 + (j - P)]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + u * step;
+      if (j < L) kv_indices[base + j] = v[u];
+    }
+  }
 }
 
 // grid (chunks, batch)
